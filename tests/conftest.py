@@ -1,0 +1,12 @@
+"""pytest configuration: the `gpu` marker and the repository root on sys.path."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line(
+        "markers", "gpu: needs a GB300 (sm_103) GPU and the compiled CUDA library")

@@ -1,0 +1,52 @@
+"""Error metrics for comparing a GEMM result with the fp64 oracle.
+
+The bar: every element within 2 ulps of the output type at |ref| plus an
+absolute 1e-3, and a relative Frobenius error of at most 1e-3.  The ulp is
+the spacing of the output format in the binade of |ref|:
+  fp16:  2^(floor(log2|x|) - 10) for |x| >= 2^-14, else 2^-24;
+  bf16:  2^(floor(log2|x|) - 7)  for |x| >= 2^-126, else 2^-133.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_FMT = {"f16": (10, -14), "bf16": (7, -126)}
+
+ULPS = 2.0
+ABS = 1e-3
+FROB = 1e-3
+
+
+def ulp(x, dtype: str) -> np.ndarray:
+    mant, emin = _FMT[dtype]
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        _, e = np.frexp(a)                  # a = f * 2^e, f in [0.5, 1)
+    floor_log2 = e.astype(np.int64) - 1
+    q = np.where(a >= np.ldexp(1.0, emin), floor_log2 - mant, emin - mant)
+    return np.ldexp(1.0, q)
+
+
+def compare(got, ref, dtype: str, ulps: float = ULPS, abs_tol: float = ABS):
+    """Return a dict of error statistics; `ok` is the pass/fail verdict."""
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if g.size == 0:
+        return {"ok": True, "max_abs": 0.0, "max_ulp": 0.0, "frob": 0.0, "bad": 0}
+    err = np.abs(g - r)
+    u = ulp(r, dtype)
+    bound = ulps * u + abs_tol
+    finite = np.isfinite(g)
+    bad = (~finite) | (err > bound)
+    nr = np.linalg.norm(r)
+    frob = float(np.linalg.norm(np.where(finite, g - r, np.inf)) / nr) if nr > 0 else float(
+        np.linalg.norm(g - r))
+    return {
+        "ok": bool((not bad.any()) and frob <= FROB),
+        "max_abs": float(np.max(np.where(finite, err, np.inf))),
+        "max_ulp": float(np.max(np.where(finite, err / u, np.inf))),
+        "frob": frob,
+        "bad": int(bad.sum()),
+        "first_bad": (tuple(int(i) for i in np.argwhere(bad)[0]) if bad.any() else None),
+    }
