@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 software-pipelined tiled GEMM.
+
+Default workload: fp16 C = A.B^T at M = N = K = 8192, entries N(0,1)/sqrt(K)
+from seed 2, fp32 accumulation, fp16 output, pipelined kernel.  One step is
+one full GEMM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--stages S] [--variant pipelined|single_buffer]
+
+--impl reference times the CPU oracle (fp64, OpenMP) on a bounded sample of
+the same workload: a block of output rows per step.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own independent
+replica of the workload (the GEMM has no exchange step); the job's value is
+all ranks' flops over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gemm_inputs  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (2MNK/time) at fp16 8192^3 on 1 GB300; % of dense tensor-core peak"
+UNIT = "TFLOP/s"
+FALLBACK_TFLOPS = 1900.0
+FALLBACK_HBM = 6800.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemm_8192_f16", choices=sorted(gemm_inputs.WORKLOADS))
+    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--variant", default="pipelined", choices=["pipelined", "single_buffer"])
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--raster-group", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_TFLOPS, "bf16_tflops_sustained": 1700.0,
+                "hbm_gbs": FALLBACK_HBM}, "fallback"
+
+
+def source_digest():
+    from software_pipelined_tiled_gemm_gb300 import _build
+    return _build._digest()
+
+
+def traffic_from_profiles(workload, digest):
+    """DRAM bytes per launch of the GEMM kernel from a committed ncu summary,
+    if that summary was taken on the current kernel sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as f:
+            for line in f:
+                if not line.startswith("bench-traffic:"):
+                    continue
+                kv = dict(x.split("=", 1) for x in line.split()[1:] if "=" in x)
+                if kv.get("workload") == workload and kv.get("source_digest") == digest:
+                    try:
+                        return int(kv["dram_bytes_per_launch"])
+                    except (KeyError, ValueError):
+                        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.strip().split(",") for r in self.tmp.read().splitlines() if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for i, n in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, pw) if p > 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+def cpu_baseline(A, B, w, seconds, threads=0):
+    """Time the oracle (as it is) on a block of output rows of this workload."""
+    import oracle
+    oracle.build()
+    epi = None if w.epilogue == "none" else "gelu"
+    # calibrate on a few rows, then size the sample to about `seconds`
+    probe = max(1, min(w.M, max(2, oracle.max_threads())))
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A[:probe], B, w.dtype, epilogue=epi, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rows = int(max(1, min(w.M, probe * seconds / dt)))
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A[:rows], B, w.dtype, epilogue=epi, threads=threads)
+    el = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d output rows (all %d columns, full K=%d), %.1f s" % (
+                rows, w.M, w.N, w.K, el)}, rows
+
+
+def run_reference(args, w, ws, rank):
+    """CPU oracle arm: each step computes a bounded block of output rows."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    A, B = gemm_inputs.make(w)
+    epi = None if w.epilogue == "none" else "gelu"
+    total_steps = args.steps + args.warmup
+    per_step = max(0.5, min(8.0, 150.0 / max(total_steps, 1)))
+    probe = max(1, min(w.M, max(2, oracle.max_threads())))
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A[:probe], B, w.dtype, epilogue=epi)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rows = int(max(1, min(w.M, probe * per_step / dt)))
+    for i in range(args.warmup):
+        oracle.gemm_nt(A[(i * rows) % w.M:][:rows], B, w.dtype, epilogue=epi)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm_nt(A[(i * rows) % w.M:][:rows], B, w.dtype, epilogue=epi)
+    el = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "input_dtype": w.dtype,
+                   "epilogue": w.epilogue, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": "%d of %d output rows per step (all columns, full K)" % (rows, w.M)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    w = gemm_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    import torch
+    import torch.distributed as dist
+    import software_pipelined_tiled_gemm_gb300 as sg
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    epi = None if w.epilogue == "none" else "gelu"
+    A_cpu, B_cpu = gemm_inputs.make(w)
+    A, B = A_cpu.to(dev), B_cpu.to(dev)
+    C = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
+    plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
+                   tile_n=args.tile_n, raster_group=args.raster_group)
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            plan.run_ptr(a_p, b_p, c_p, sptr)
+    stream.synchronize()
+    ds, detail = plan.check()
+    if ds != 0:
+        raise SystemExit("device status %d (detail %#x) after warm-up" % (ds, detail))
+    info = plan.info()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(args.steps):
+        ks[i].record(stream)
+        plan.run_ptr(a_p, b_p, c_p, sptr)
+        ke[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    kern_ms = [a.elapsed_time(b) for a, b in zip(ks, ke)]
+    ds, detail = plan.check()
+    if ds != 0:
+        raise SystemExit("device status %d (detail %#x) after timed steps" % (ds, detail))
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    flops = 2.0 * w.M * w.N * w.K
+    value = flops * args.steps * ws / (elapsed_ms * 1e-3) / 1e12
+    kavg = sum(kern_ms) / len(kern_ms)
+    achieved = flops / (kavg * 1e-3) / 1e12
+
+    # end-to-end through the C ABI with host buffers (pinned)
+    e2e = None
+    if args.e2e_steps > 0:
+        hA, hB = A_cpu.pin_memory(), B_cpu.pin_memory()
+        hC = torch.empty(w.M, w.N, dtype=A_cpu.dtype).pin_memory()
+        eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
+                        tile_n=args.tile_n, raster_group=args.raster_group)
+        eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
+        el = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([el], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            el = float(t.item())
+        eplan.close()
+        e2e = {"value": flops * args.e2e_steps * ws / el / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": (w.M * w.K + w.N * w.K) * 2,
+               "d2h_bytes_per_step": w.M * w.N * 2}
+
+    peaks, peak_src = load_peaks()
+    sustained = elapsed_ms > 1000.0
+    peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = float(peaks.get(peak_key, FALLBACK_TFLOPS))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM))
+    digest = source_digest()
+    traffic = traffic_from_profiles(w.name, digest)
+    min_bytes = 2.0 * (w.M * w.K + w.N * w.K + w.M * w.N)
+    # Below the ridge point (peak flops / HBM bandwidth) the GEMM is bound by
+    # moving its operands once; report it against the copy bandwidth.
+    if flops / min_bytes < peak * 1e12 / (hbm * 1e9):
+        roof = {"bound": "hbm", "achieved": min_bytes / (kavg * 1e-3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "traffic": traffic,
+                "peak_source": "%s hbm_gbs" % peak_src,
+                "tensor_tflops": achieved, "kernel_ms_avg": kavg}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "traffic": traffic,
+                "peak_source": "%s %s (fp16 and bf16 share the dense tensor rate)" % (
+                    peak_src, peak_key),
+                "kernel_ms_avg": kavg}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        cpu, _ = cpu_baseline(A_cpu, B_cpu, w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {
+                "workload": w.name, "M": w.M, "N": w.N, "K": w.K, "input_dtype": w.dtype,
+                "accumulate": "f32", "epilogue": w.epilogue, "variant": args.variant,
+                "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
+                                                               info["tile_k"]),
+                "grid": info["grid"], "raster_group": info["raster_group"],
+                "l2": ("inputs larger than L2 (%d MiB of operands vs %d MiB L2); no flush"
+                       % ((w.M * w.K + w.N * w.K) * 2 >> 20, L2_BYTES >> 20))
+                if (w.M * w.K + w.N * w.K) * 2 > L2_BYTES else "operands fit in L2 (warm)",
+                "parallelism": "replicas" if ws > 1 else "single-gpu",
+            },
+            "roofline": roof,
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": args.steps * info["kernels_per_run"],
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

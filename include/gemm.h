@@ -1,0 +1,182 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) software-pipelined tiled GEMM.
+ *
+ *   C[i,j] = epi( sum_k A[i,k] * B[j,k] ),   0 <= i < M, 0 <= j < N
+ *
+ * Operation.  TileLang tutorial, chapter 11 ("Pipelining and autotuning"),
+ * pipelined_gemm.py, kernel matmul_auto: A is an (M, K) tensor, B an (N, K)
+ * tensor, C an (M, N) tensor; every (block_M, block_N) output tile clears a
+ * float32 accumulator, walks the K dimension in block_K slices through a
+ * num_stages-deep pipeline and multiplies with T.gemm(..., transpose_B=True);
+ * the float32 tile is then written out in the 16-bit input type.  The inputs
+ * are fp16 or bf16, the products are accumulated in fp32, and each output is
+ * rounded once, to nearest even, to the input type.
+ *
+ * Epilogue.  GEMM_EPI_GELU_TANH applies the tanh-approximate GELU
+ * 0.5 x (1 + tanh(0.7978845608 (x + 0.044715 x^3))) to the fp32 accumulator
+ * before the rounding (the form written in the Triton lecture notes' "GeLU"
+ * example and in the XLA:GPU emitters page's loop-emitter @gelu function).
+ *
+ * Pipelining.  `stages` is the depth of the shared-memory ring that the K
+ * loop streams through -- num_stages in the TileLang tutorial,
+ * max_concurrent_steps in the Mosaic GPU pipelining guide ("Pipelining with
+ * Mosaic GPU").  A ring slot is handed back to the copy engine only when the
+ * tensor-core instructions that read it have completed; this is the hazard
+ * the guide's delay_release option exists for (refilling a slot that an
+ * asynchronous matrix multiply has not finished reading).  GEMM_SINGLE_BUFFER is the tutorial's
+ * matmul_plain contrast: one slot, one accumulator, so copies and math of
+ * consecutive K slices cannot overlap.
+ *
+ * Layout.  All matrices are row-major and dense: A has K elements per row
+ * (lda = K), B has K elements per row (ldb = K), C has N elements per row
+ * (ldc = N).  Both operands are therefore K-contiguous ("K-major").
+ * Element type of A, B and C is `dtype`.  Pointers A, B, C are device
+ * pointers (cudaMalloc / torch CUDA tensors) on the plan's device, except for
+ * gemm_run_host, which takes host pointers.
+ *
+ * Partial tiles.  Any M, N >= 0 and K >= 0 is accepted.  Out-of-range rows
+ * and K columns contribute zero and out-of-range outputs are never written
+ * (the masked loads and stores of the Triton lecture notes' matmul example).
+ * When a row pitch or a base address is not 16-byte aligned, A and B are
+ * first copied into plan-owned, padded device scratch and C is written with
+ * plain masked stores instead of bulk tensor stores.
+ *
+ * Ownership.  The caller owns A, B, C and the stream.  A plan owns its
+ * device status word, its padding scratch and (after the first
+ * gemm_run_host) its device staging buffers; gemm_plan_destroy frees them.
+ *
+ * Threading.  A plan may be used from one host thread at a time and must not
+ * have launches in flight on two streams at once.  Different plans are
+ * independent.
+ *
+ * Errors.  Every entry point returns a gemm_status_t and never throws.
+ * Argument errors are detected on the host before anything is launched.
+ * Faults detected on the device (a pipeline wait that ran out its time
+ * limit) are recorded in the plan's status word and reported by
+ * gemm_plan_check.  gemm_run is asynchronous: a GEMM_OK return means the
+ * work was enqueued.
+ */
+#ifndef SPGEMM_GEMM_H_
+#define SPGEMM_GEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,   /* null/negative/out-of-range argument, aliasing C with A or B */
+  GEMM_ERR_UNSUPPORTED = 2,   /* device is not sm_103 / feature not built */
+  GEMM_ERR_SMEM_BUDGET = 3,   /* requested stages/tile do not fit the shared-memory budget */
+  GEMM_ERR_PLAN_MISMATCH = 4, /* run arguments differ from the plan's */
+  GEMM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+  GEMM_ERR_TIMEOUT = 6        /* device: a pipeline wait exceeded its time limit */
+} gemm_status_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
+
+typedef enum { GEMM_EPI_NONE = 0, GEMM_EPI_GELU_TANH = 1 } gemm_epilogue_t;
+
+typedef enum {
+  GEMM_PIPELINED = 0,     /* `stages`-deep ring, double-buffered accumulator */
+  GEMM_SINGLE_BUFFER = 1  /* one ring slot, one accumulator (no overlap) */
+} gemm_variant_t;
+
+typedef struct gemm_plan gemm_plan_t; /* opaque */
+
+/* Optional tuning knobs for gemm_plan_create_ex.  Zero means "choose". */
+typedef struct {
+  int tile_n;          /* output tile width: 0 (auto), 64, 128 or 256; tile height is 128 */
+  int raster_group;    /* tile rows walked together for L2 reuse; 0 = auto */
+  int max_ctas;        /* cap on persistent CTAs; 0 = one per SM */
+  int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
+} gemm_tuning_t;
+
+/* Read-only description of what a plan will launch (for tests and benchmarks). */
+typedef struct {
+  int tile_m, tile_n, tile_k;  /* CTA output tile and K slice */
+  int stages;                  /* ring depth actually used */
+  int accumulators;            /* TMEM accumulator buffers (1 or 2) */
+  int raster_group;
+  int grid;                    /* persistent CTAs launched */
+  int64_t num_tiles;
+  size_t smem_bytes;           /* dynamic shared memory per CTA */
+  int pads_operands;           /* last run staged A/B through padded scratch */
+  int tma_store;               /* last run stored C with bulk tensor stores */
+  int kernels_per_run;         /* kernel launches of the last run */
+  int sm_count;
+} gemm_plan_info_t;
+
+/* Create a plan for C = epi(A . B^T) of the given sizes on `device`.
+ * stages: ring depth >= 1 (GEMM_SINGLE_BUFFER requires 1).  With automatic
+ * tiling the widest output tile whose ring fits the shared-memory budget is
+ * chosen.  Returns GEMM_ERR_SMEM_BUDGET when even the narrowest tile does not
+ * fit (never clamps `stages`).  On success *out owns device memory: release
+ * it with gemm_plan_destroy.  On failure *out is set to NULL. */
+gemm_status_t gemm_plan_create(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
+                               gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                               gemm_variant_t variant, int device);
+
+/* As gemm_plan_create, with explicit tuning (tuning may be NULL). */
+gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
+                                  gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                                  gemm_variant_t variant, int device,
+                                  const gemm_tuning_t* tuning);
+
+/* Enqueue C = epi(A . B^T) on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  A, B, C: device pointers as described above; C must not overlap
+ * A or B.  M, N, K, dtype, epi and stages must equal the plan's
+ * (GEMM_ERR_PLAN_MISMATCH otherwise).  M == 0 or N == 0 is a no-op; K == 0
+ * writes zeros (GELU(0) = 0).  Asynchronous: does not synchronise the
+ * stream or the device. */
+gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
+                       int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                       gemm_epilogue_t epi, int stages, void* stream);
+
+/* End-to-end call with HOST buffers: copies hA (M*K) and hB (N*K) to
+ * plan-owned device buffers on `stream`, runs the GEMM, copies C back to hC
+ * (M*N) and synchronises `stream` before returning.  Pinned host memory gives
+ * asynchronous copies; pageable memory works too.  The first call allocates
+ * the device buffers. */
+gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, void* hC,
+                            int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                            gemm_epilogue_t epi, int stages, void* stream);
+
+/* Synchronise the plan's device and read (then clear) its device status word.
+ * *device_status receives GEMM_OK or the code a kernel recorded (e.g.
+ * GEMM_ERR_TIMEOUT); *detail (may be NULL) receives the place it was recorded
+ * (role << 16 | wait id).  Returns GEMM_ERR_CUDA if the synchronisation
+ * itself failed. */
+gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t* detail);
+
+/* Describe the plan's launch configuration. */
+gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info);
+
+/* Free everything the plan owns.  NULL is allowed.  Waits for the plan's
+ * device work to finish first. */
+void gemm_plan_destroy(gemm_plan_t* plan);
+
+/* Static text for a status code ("GEMM_OK", ...). */
+const char* gemm_status_string(gemm_status_t s);
+
+/* Last error message recorded by this host thread (argument that failed,
+ * CUDA error text), or "" if none.  The pointer stays valid until the next
+ * call into this library from the same thread. */
+const char* gemm_last_error(void);
+
+/* Shared-memory bytes of the operand ring, the TileLang tutorial's
+ * shared_bytes(): stages * (bm*bk + bn*bk) * elem_bytes.  Returns 0 if an
+ * argument is not positive. */
+size_t gemm_smem_bytes(int bm, int bn, int bk, int elem_bytes, int stages);
+
+/* Library version as "major.minor.patch". */
+const char* gemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPGEMM_GEMM_H_ */

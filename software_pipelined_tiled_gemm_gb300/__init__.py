@@ -1,0 +1,323 @@
+"""GB300 (sm_103a) software-pipelined tiled GEMM: C = epi(A . B^T).
+
+A thin ctypes binding over the C ABI in ``include/gemm.h`` (library
+``_lib/libspgemm.so``).  The functions ``gemm_plan_create``,
+``gemm_plan_create_ex``, ``gemm_run``, ``gemm_run_host``, ``gemm_plan_check``,
+``gemm_plan_get_info``, ``gemm_plan_destroy``, ``gemm_status_string``,
+``gemm_smem_bytes`` carry the C names and only marshal arguments; every step of
+the GEMM runs in the library's CUDA kernels.  PyTorch is used for device
+memory and the current stream only.
+
+There is no fallback: if the library is missing or cannot be loaded, every
+call raises.
+
+Convenience layer: :func:`matmul_nt` takes torch CUDA tensors A (M,K) and
+B (N,K), caches a plan per problem, and launches on the current stream --
+the operation of the TileLang tutorial's ``matmul_auto`` (A (M,K), B (N,K),
+``T.gemm(..., transpose_B=True)``) with an optional tanh-GELU epilogue.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "GemmError", "Plan", "matmul_nt", "load_library", "library_path",
+    "gemm_plan_create", "gemm_plan_create_ex", "gemm_run", "gemm_run_host", "gemm_plan_check",
+    "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
+    "gemm_last_error", "gemm_version", "GemmTuning", "GemmPlanInfo",
+    "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
+    "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
+    "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH",
+    "GEMM_PIPELINED", "GEMM_SINGLE_BUFFER",
+]
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "_lib", "libspgemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_SMEM_BUDGET = 3
+GEMM_ERR_PLAN_MISMATCH = 4
+GEMM_ERR_CUDA = 5
+GEMM_ERR_TIMEOUT = 6
+
+GEMM_F16 = 0
+GEMM_BF16 = 1
+GEMM_EPI_NONE = 0
+GEMM_EPI_GELU_TANH = 1
+GEMM_PIPELINED = 0
+GEMM_SINGLE_BUFFER = 1
+
+
+class GemmTuning(ctypes.Structure):
+    _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
+                ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_int64)]
+
+
+class GemmPlanInfo(ctypes.Structure):
+    _fields_ = [("tile_m", ctypes.c_int), ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int),
+                ("stages", ctypes.c_int), ("accumulators", ctypes.c_int),
+                ("raster_group", ctypes.c_int), ("grid", ctypes.c_int),
+                ("num_tiles", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t),
+                ("pads_operands", ctypes.c_int), ("tma_store", ctypes.c_int),
+                ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = _status_name(status)
+        super().__init__("%s: %s%s" % (where, name, (" -- " + detail) if detail else ""))
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: Optional[str] = None):
+    """Load libspgemm.so (building it first if the sources are newer)."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if path is None:
+            from . import _build
+            if not _build.up_to_date():
+                _build.build()
+            path = _LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError("libspgemm.so not found at %s; run __graft_entry__.build()" % path)
+        lib = ctypes.CDLL(path)
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        lib.gemm_plan_create.argtypes = [pp, i64, i64, i64, ci, ci, ci, ci, ci]
+        lib.gemm_plan_create.restype = ci
+        lib.gemm_plan_create_ex.argtypes = [pp, i64, i64, i64, ci, ci, ci, ci, ci,
+                                            ctypes.POINTER(GemmTuning)]
+        lib.gemm_plan_create_ex.restype = ci
+        lib.gemm_run.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
+        lib.gemm_run.restype = ci
+        lib.gemm_run_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
+        lib.gemm_run_host.restype = ci
+        lib.gemm_plan_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
+                                        ctypes.POINTER(ctypes.c_int32)]
+        lib.gemm_plan_check.restype = ci
+        lib.gemm_plan_get_info.argtypes = [vp, ctypes.POINTER(GemmPlanInfo)]
+        lib.gemm_plan_get_info.restype = ci
+        lib.gemm_plan_destroy.argtypes = [vp]
+        lib.gemm_plan_destroy.restype = None
+        lib.gemm_status_string.argtypes = [ci]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_last_error.argtypes = []
+        lib.gemm_last_error.restype = ctypes.c_char_p
+        lib.gemm_smem_bytes.argtypes = [ci, ci, ci, ci, ci]
+        lib.gemm_smem_bytes.restype = ctypes.c_size_t
+        lib.gemm_version.argtypes = []
+        lib.gemm_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load_library().gemm_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - naming only
+        return "status %d" % status
+
+
+def _check(status: int, where: str):
+    if status != GEMM_OK:
+        raise GemmError(status, where, load_library().gemm_last_error().decode())
+
+
+# ------------------------------------------------------- C-named wrappers --
+
+def gemm_status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def gemm_last_error() -> str:
+    return load_library().gemm_last_error().decode()
+
+
+def gemm_version() -> str:
+    return load_library().gemm_version().decode()
+
+
+def gemm_smem_bytes(bm: int, bn: int, bk: int, elem_bytes: int, stages: int) -> int:
+    return int(load_library().gemm_smem_bytes(bm, bn, bk, elem_bytes, stages))
+
+
+def gemm_plan_create(M, N, K, dtype, epi, stages, variant, device):
+    """Returns (status, plan_handle_or_None)."""
+    h = ctypes.c_void_p()
+    st = load_library().gemm_plan_create(ctypes.byref(h), M, N, K, dtype, epi, stages, variant,
+                                         device)
+    return st, (h.value if st == GEMM_OK else None)
+
+
+def gemm_plan_create_ex(M, N, K, dtype, epi, stages, variant, device, tuning=None):
+    h = ctypes.c_void_p()
+    tp = ctypes.byref(tuning) if tuning is not None else None
+    st = load_library().gemm_plan_create_ex(ctypes.byref(h), M, N, K, dtype, epi, stages,
+                                            variant, device, tp)
+    return st, (h.value if st == GEMM_OK else None)
+
+
+def gemm_run(plan, A, B, C, M, N, K, dtype, epi, stages, stream):
+    """A, B, C, stream: integer addresses / handles.  Returns the status."""
+    return load_library().gemm_run(plan, A, B, C, M, N, K, dtype, epi, stages, stream)
+
+
+def gemm_run_host(plan, hA, hB, hC, M, N, K, dtype, epi, stages, stream):
+    return load_library().gemm_run_host(plan, hA, hB, hC, M, N, K, dtype, epi, stages, stream)
+
+
+def gemm_plan_check(plan):
+    """Returns (status, device_status, detail)."""
+    ds, dt = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = load_library().gemm_plan_check(plan, ctypes.byref(ds), ctypes.byref(dt))
+    return st, ds.value, dt.value
+
+
+def gemm_plan_get_info(plan):
+    info = GemmPlanInfo()
+    st = load_library().gemm_plan_get_info(plan, ctypes.byref(info))
+    return st, info
+
+
+def gemm_plan_destroy(plan):
+    load_library().gemm_plan_destroy(plan)
+
+
+# ------------------------------------------------------------ torch layer --
+
+_DT = {"f16": GEMM_F16, "bf16": GEMM_BF16}
+_EPI = {None: GEMM_EPI_NONE, "none": GEMM_EPI_NONE, "gelu": GEMM_EPI_GELU_TANH,
+        "gelu_tanh": GEMM_EPI_GELU_TANH}
+_VAR = {"pipelined": GEMM_PIPELINED, "single_buffer": GEMM_SINGLE_BUFFER}
+
+
+def _torch_dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return GEMM_F16
+    if t.dtype == torch.bfloat16:
+        return GEMM_BF16
+    raise TypeError("A and B must be float16 or bfloat16, got %s" % t.dtype)
+
+
+class Plan:
+    """Owns one gemm_plan_t."""
+
+    def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
+                 tile_n=0, raster_group=0, max_ctas=0, timeout_ns=0):
+        self.M, self.N, self.K = int(M), int(N), int(K)
+        self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
+        self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
+        self.stages = int(stages)
+        self.variant = _VAR[variant] if isinstance(variant, str) else int(variant)
+        self.device = int(device)
+        self._h = None
+        tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(timeout_ns))
+        st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
+                                    self.variant, self.device, tuning)
+        _check(st, "gemm_plan_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> dict:
+        st, info = gemm_plan_get_info(self._h)
+        _check(st, "gemm_plan_get_info")
+        return info.as_dict()
+
+    def run_ptr(self, A: int, B: int, C: int, stream: int = 0):
+        _check(gemm_run(self._h, A, B, C, self.M, self.N, self.K, self.dtype, self.epi,
+                        self.stages, stream), "gemm_run")
+
+    def run(self, A, B, C, stream=None):
+        """A, B, C: torch CUDA tensors (contiguous, shapes (M,K), (N,K), (M,N))."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(A.device)
+        self.run_ptr(A.data_ptr(), B.data_ptr(), C.data_ptr(), s.cuda_stream)
+
+    def run_host(self, hA: int, hB: int, hC: int, stream: int = 0):
+        _check(gemm_run_host(self._h, hA, hB, hC, self.M, self.N, self.K, self.dtype, self.epi,
+                             self.stages, stream), "gemm_run_host")
+
+    def check(self):
+        """Synchronise and return (device_status, detail); raises on a device error."""
+        st, ds, detail = gemm_plan_check(self._h)
+        _check(st, "gemm_plan_check")
+        return ds, detail
+
+    def close(self):
+        if self._h is not None:
+            gemm_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+
+_plans = {}
+_plans_lock = threading.Lock()
+
+
+def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
+             **tuning) -> Plan:
+    key = (M, N, K, dtype, epilogue, stages, variant, device, tuple(sorted(tuning.items())))
+    with _plans_lock:
+        p = _plans.get(key)
+        if p is None:
+            p = Plan(M, N, K, dtype, epilogue, stages, variant, device, **tuning)
+            _plans[key] = p
+        return p
+
+
+def matmul_nt(A, B, epilogue=None, stages: int = 4, variant: str = "pipelined", out=None,
+              **tuning):
+    """C = epi(A @ B.T) on the current CUDA stream.
+
+    A: (M, K) and B: (N, K) CUDA tensors of the same dtype (float16 or
+    bfloat16), contiguous.  Returns C (M, N) of that dtype (``out`` if given).
+    """
+    import torch
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be (M, K) and B (N, K) with the same K")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    if A.device != B.device:
+        raise ValueError("A and B must be on the same device")
+    dt = _torch_dtype_code(A)
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    elif out.shape != (M, N) or out.dtype != A.dtype or not out.is_contiguous() or out.device != A.device:
+        raise ValueError("out must be a contiguous (M, N) tensor of A's dtype on A's device")
+    dtype = "bf16" if dt == GEMM_BF16 else "f16"
+    plan = get_plan(M, N, K, dtype, epilogue, stages, variant, A.device.index or 0, **tuning)
+    plan.run(A, B, out)
+    return out

@@ -1,0 +1,569 @@
+// gemm_api.cu -- the C ABI declared in include/gemm.h: argument checking,
+// tile/ring planning, tensor-map encoding, launches and error reporting.
+//
+// The planner follows the TileLang tutorial's shared-memory budget
+// (pipelined_gemm.py, shared_bytes(): stages * (block_M*block_K +
+// block_N*block_K) * element size, checked against the device limit the way
+// its main() marks a depth "OVER"), plus the epilogue staging and barrier
+// bytes this kernel adds on top.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/gemm.h"
+#include "kernel_params.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+using namespace spgemm;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gemm_status_t fail(gemm_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+gemm_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(GEMM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+  int prev = -1;
+  bool switched = false;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) {
+      err = cudaSetDevice(dev);
+      switched = err == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (switched) cudaSetDevice(prev);
+  }
+};
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+}  // namespace
+
+struct gemm_plan {
+  int device = 0;
+  int64_t M = 0, N = 0, K = 0;
+  gemm_dtype_t dtype = GEMM_F16;
+  gemm_epilogue_t epi = GEMM_EPI_NONE;
+  int stages = 0;
+  gemm_variant_t variant = GEMM_PIPELINED;
+
+  int sm_count = 0;
+  int bn = 256;
+  int num_acc = 2;
+  int store_bufs = 2;
+  int raster_group = 16;
+  int grid = 0;
+  int max_ctas = 0;
+  int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
+  size_t smem = 0;
+  unsigned long long timeout_ns = kDefaultTimeoutNs;
+
+  int* d_status = nullptr;       // [0] code, [1] detail
+  uint16_t* scratch = nullptr;   // padded copies of A and/or B
+  size_t scratch_bytes = 0;
+
+  // tensor-map cache, keyed by the pointers/pitches they were encoded for
+  const void* mapA_ptr = nullptr;
+  const void* mapB_ptr = nullptr;
+  const void* mapC_ptr = nullptr;
+  int64_t mapK = -1;
+  CUtensorMap tmA{}, tmB{}, tmC{};
+
+  // device staging for gemm_run_host
+  void* hA = nullptr;
+  void* hB = nullptr;
+  void* hC = nullptr;
+
+  int last_pads = 0;
+  int last_tma_store = 0;
+  int last_kernels = 0;
+};
+
+namespace {
+
+gemm_status_t encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* base, int64_t inner,
+                        int64_t rows, int64_t pitch_elems, uint32_t box_inner, uint32_t box_rows,
+                        CUtensorMapL2promotion l2) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2u};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapDataType t =
+      dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for %lld x %lld",
+                static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(inner));
+  return GEMM_OK;
+}
+
+gemm_status_t check_common(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                           gemm_epilogue_t epi, int stages) {
+  if (M < 0 || N < 0 || K < 0)
+    return fail(GEMM_ERR_INVALID_ARG, "negative size M=%lld N=%lld K=%lld", (long long)M,
+                (long long)N, (long long)K);
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(GEMM_ERR_INVALID_ARG, "size above 2^31-1");
+  if (dtype != GEMM_F16 && dtype != GEMM_BF16)
+    return fail(GEMM_ERR_INVALID_ARG, "dtype %d out of range", static_cast<int>(dtype));
+  if (epi != GEMM_EPI_NONE && epi != GEMM_EPI_GELU_TANH)
+    return fail(GEMM_ERR_INVALID_ARG, "epilogue %d out of range", static_cast<int>(epi));
+  if (stages < 1 || stages > kMaxStages)
+    return fail(GEMM_ERR_INVALID_ARG, "stages %d outside [1, %d]", stages, kMaxStages);
+  return GEMM_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+cudaError_t set_smem(int bn, size_t smem) {
+  switch (bn) {
+    case 64: return gemm_set_smem_bn64(smem);
+    case 128: return gemm_set_smem_bn128(smem);
+    default: return gemm_set_smem_bn256(smem);
+  }
+}
+
+cudaError_t launch(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                   const Params& p, int grid, size_t smem, cudaStream_t s) {
+  switch (bn) {
+    case 64: return gemm_launch_bn64(a, b, c, p, grid, smem, s);
+    case 128: return gemm_launch_bn128(a, b, c, p, grid, smem, s);
+    default: return gemm_launch_bn256(a, b, c, p, grid, smem, s);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_SMEM_BUDGET: return "GEMM_ERR_SMEM_BUDGET";
+    case GEMM_ERR_PLAN_MISMATCH: return "GEMM_ERR_PLAN_MISMATCH";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+  }
+  return "GEMM_ERR_UNKNOWN";
+}
+
+const char* gemm_last_error(void) { return g_last_error.c_str(); }
+
+const char* gemm_version(void) { return "0.1.0"; }
+
+size_t gemm_smem_bytes(int bm, int bn, int bk, int elem_bytes, int stages) {
+  if (bm <= 0 || bn <= 0 || bk <= 0 || elem_bytes <= 0 || stages <= 0) return 0;
+  return static_cast<size_t>(stages) *
+         (static_cast<size_t>(bm) * bk + static_cast<size_t>(bn) * bk) *
+         static_cast<size_t>(elem_bytes);
+}
+
+gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
+                                  gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                                  gemm_variant_t variant, int device,
+                                  const gemm_tuning_t* tuning) {
+  g_last_error.clear();
+  if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  gemm_status_t st = check_common(M, N, K, dtype, epi, stages);
+  if (st != GEMM_OK) return st;
+  if (variant != GEMM_PIPELINED && variant != GEMM_SINGLE_BUFFER)
+    return fail(GEMM_ERR_INVALID_ARG, "variant %d out of range", static_cast<int>(variant));
+  if (variant == GEMM_SINGLE_BUFFER && stages != 1)
+    return fail(GEMM_ERR_INVALID_ARG, "the single-buffer variant has exactly 1 stage (got %d)",
+                stages);
+  if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
+  int want_bn = 0, want_group = 0, want_ctas = 0;
+  unsigned long long timeout = kDefaultTimeoutNs;
+  if (tuning) {
+    want_bn = tuning->tile_n;
+    want_group = tuning->raster_group;
+    want_ctas = tuning->max_ctas;
+    if (want_bn != 0 && want_bn != 64 && want_bn != 128 && want_bn != 256)
+      return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", want_bn);
+    if (want_group < 0 || want_ctas < 0)
+      return fail(GEMM_ERR_INVALID_ARG, "negative raster_group / max_ctas");
+    if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
+    if (tuning->timeout_ns > 0) timeout = static_cast<unsigned long long>(tuning->timeout_ns);
+  }
+
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device >= ndev) return fail(GEMM_ERR_INVALID_ARG, "device %d >= count %d", device, ndev);
+  DeviceGuard guard(device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(GEMM_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                device, prop.major, prop.minor);
+  int smem_optin = 0;
+  e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem optin)");
+
+  gemm_plan* p = new (std::nothrow) gemm_plan();
+  if (!p) return fail(GEMM_ERR_INVALID_ARG, "out of host memory");
+  p->device = device;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->dtype = dtype;
+  p->epi = epi;
+  p->stages = stages;
+  p->variant = variant;
+  p->sm_count = prop.multiProcessorCount;
+  p->timeout_ns = timeout;
+  p->num_acc = variant == GEMM_SINGLE_BUFFER ? 1 : 2;
+  p->max_ctas = want_ctas;
+
+  // Tile width: explicit, or the widest that fits the budget, narrowed while
+  // the widest leaves most SMs idle (fewer tiles than SMs).
+  const int cands[3] = {256, 128, 64};
+  int chosen = 0;
+  size_t chosen_smem = 0;
+  int chosen_bufs = 0;
+  const int64_t tm = cdiv(std::max<int64_t>(M, 1), kBM);
+  for (int i = 0; i < 3; ++i) {
+    const int bn = cands[i];
+    if (want_bn != 0 && bn != want_bn) continue;
+    int bufs = 2;
+    size_t need = kernel_smem_bytes(bn, stages, bufs);
+    if (need > static_cast<size_t>(smem_optin)) {
+      bufs = 1;
+      need = kernel_smem_bytes(bn, stages, bufs);
+    }
+    if (need > static_cast<size_t>(smem_optin)) continue;
+    const int64_t tiles = tm * cdiv(std::max<int64_t>(N, 1), bn);
+    chosen = bn;
+    chosen_smem = need;
+    chosen_bufs = bufs;
+    if (want_bn != 0 || tiles >= p->sm_count) break;
+  }
+  if (chosen == 0) {
+    delete p;
+    return fail(GEMM_ERR_SMEM_BUDGET,
+                "stages=%d does not fit %d B of shared memory at tile width %d (ring %zu B)",
+                stages, smem_optin, want_bn ? want_bn : 64,
+                gemm_smem_bytes(kBM, want_bn ? want_bn : 64, kBK, 2, stages));
+  }
+  p->bn = chosen;
+  p->smem = chosen_smem;
+  p->store_bufs = chosen_bufs;
+  p->tiles_m = cdiv(M, kBM);
+  p->tiles_n = cdiv(N, chosen);
+  p->num_tiles = p->tiles_m * p->tiles_n;
+  if (p->num_tiles > kMaxDim) {
+    delete p;
+    return fail(GEMM_ERR_INVALID_ARG, "too many output tiles");
+  }
+  p->raster_group = want_group > 0 ? want_group : 16;
+  if (p->tiles_m > 0) p->raster_group = static_cast<int>(std::min<int64_t>(p->raster_group, p->tiles_m));
+  int cap = p->sm_count;
+  if (want_ctas > 0) cap = std::min(cap, want_ctas);
+  p->grid = static_cast<int>(std::min<int64_t>(p->num_tiles, cap));
+
+  e = set_smem(p->bn, p->smem);
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+  }
+  e = cudaMalloc(&p->d_status, 4 * sizeof(int));
+  if (e != cudaSuccess) {
+    delete p;
+    return cuda_fail(e, "cudaMalloc(status)");
+  }
+  e = cudaMemset(p->d_status, 0, 4 * sizeof(int));
+  if (e != cudaSuccess) {
+    cudaFree(p->d_status);
+    delete p;
+    return cuda_fail(e, "cudaMemset(status)");
+  }
+  *out = p;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
+                               gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                               gemm_variant_t variant, int device) {
+  return gemm_plan_create_ex(out, M, N, K, dtype, epi, stages, variant, device, nullptr);
+}
+
+gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C, int64_t M,
+                       int64_t N, int64_t K, gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                       void* stream_handle) {
+  g_last_error.clear();
+  if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+  gemm_status_t st = check_common(M, N, K, dtype, epi, stages);
+  if (st != GEMM_OK) return st;
+  if (M != plan->M || N != plan->N || K != plan->K || dtype != plan->dtype || epi != plan->epi ||
+      stages != plan->stages)
+    return fail(GEMM_ERR_PLAN_MISMATCH,
+                "run (M=%lld N=%lld K=%lld dtype=%d epi=%d stages=%d) differs from the plan "
+                "(M=%lld N=%lld K=%lld dtype=%d epi=%d stages=%d)",
+                (long long)M, (long long)N, (long long)K, (int)dtype, (int)epi, stages,
+                (long long)plan->M, (long long)plan->N, (long long)plan->K, (int)plan->dtype,
+                (int)plan->epi, plan->stages);
+  if (M == 0 || N == 0) {
+    plan->last_kernels = 0;
+    return GEMM_OK;
+  }
+  if (!C) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
+  if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+  const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
+  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  if (ranges_overlap(C, bytesC, A, bytesA) || ranges_overlap(C, bytesC, B, bytesB))
+    return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 1u)
+    return fail(GEMM_ERR_INVALID_ARG, "A, B and C must be 2-byte aligned");
+
+  DeviceGuard guard(plan->device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_handle);
+
+  if (K == 0) {  // empty reduction: C = 0, and GELU(0) = 0
+    cudaError_t e = cudaMemsetAsync(C, 0, bytesC, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    plan->last_kernels = 0;
+    return GEMM_OK;
+  }
+
+  // Operands whose pitch or base is not 16-byte aligned go through padded scratch.
+  const bool padA = (K % 8) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
+  const bool padB = (K % 8) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
+  const int64_t Kp = (K + 7) / 8 * 8;
+  const void* effA = A;
+  const void* effB = B;
+  int kernels = 0;
+  if (padA || padB) {
+    const size_t need = ((padA ? M : 0) + (padB ? N : 0)) * static_cast<size_t>(Kp) * 2;
+    if (need > plan->scratch_bytes) {
+      if (plan->scratch) {
+        cudaError_t e = cudaFree(plan->scratch);
+        plan->scratch = nullptr;
+        plan->scratch_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(scratch)");
+      }
+      cudaError_t e = cudaMalloc(&plan->scratch, need);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
+      plan->scratch_bytes = need;
+      plan->mapA_ptr = plan->mapB_ptr = nullptr;
+    }
+    uint16_t* Ap = padA ? plan->scratch : nullptr;
+    uint16_t* Bp = padB ? plan->scratch + (padA ? M * Kp : 0) : nullptr;
+    cudaError_t e = launch_pad_operands(static_cast<const uint16_t*>(A), M, Ap,
+                                        static_cast<const uint16_t*>(B), N, Bp, K, Kp,
+                                        plan->sm_count, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
+    ++kernels;
+    if (padA) effA = Ap;
+    if (padB) effB = Bp;
+  }
+  const int64_t Keff = (padA || padB) ? Kp : K;
+  // If only one operand is padded, the other's pitch is K == Kp (K % 8 == 0).
+
+  const bool tma_store = (N % 8) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+
+  if (plan->mapA_ptr != effA || plan->mapK != Keff) {
+    st = encode_2d(&plan->tmA, plan->dtype, effA, Keff, M, Keff, kBK, kBM,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (st != GEMM_OK) return st;
+    plan->mapA_ptr = effA;
+  }
+  if (plan->mapB_ptr != effB || plan->mapK != Keff) {
+    st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
+                   static_cast<uint32_t>(plan->bn), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (st != GEMM_OK) return st;
+    plan->mapB_ptr = effB;
+  }
+  plan->mapK = Keff;
+  if (tma_store && plan->mapC_ptr != C) {
+    st = encode_2d(&plan->tmC, plan->dtype, C, N, M, N, kStoreCols, 32,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (st != GEMM_OK) return st;
+    plan->mapC_ptr = C;
+  }
+
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.M = static_cast<int>(M);
+  prm.N = static_cast<int>(N);
+  prm.K = static_cast<int>(Keff);
+  prm.tiles_m = static_cast<int>(plan->tiles_m);
+  prm.tiles_n = static_cast<int>(plan->tiles_n);
+  prm.num_tiles = static_cast<int>(plan->num_tiles);
+  prm.k_blocks = static_cast<int>(cdiv(Keff, kBK));
+  prm.stages = plan->stages;
+  prm.num_acc = plan->num_acc;
+  int cols = plan->bn * plan->num_acc;
+  int pow2 = 32;
+  while (pow2 < cols) pow2 <<= 1;
+  prm.tmem_cols = pow2;
+  prm.raster_group = plan->raster_group;
+  prm.store_bufs = plan->store_bufs;
+  prm.bf16 = plan->dtype == GEMM_BF16 ? 1 : 0;
+  prm.gelu = plan->epi == GEMM_EPI_GELU_TANH ? 1 : 0;
+  prm.tma_store = tma_store ? 1 : 0;
+  prm.idesc = ptx::instr_desc_f16(kBM, plan->bn, plan->dtype == GEMM_BF16);
+  prm.C = C;
+  prm.ldc = N;
+  prm.status = plan->d_status;
+  prm.timeout_ns = plan->timeout_ns;
+
+  cudaError_t e = launch(plan->bn, plan->tmA, plan->tmB, plan->tmC, prm, plan->grid, plan->smem,
+                         stream);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+  ++kernels;
+  plan->last_pads = (padA || padB) ? 1 : 0;
+  plan->last_tma_store = tma_store ? 1 : 0;
+  plan->last_kernels = kernels;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, void* hC,
+                            int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                            gemm_epilogue_t epi, int stages, void* stream_handle) {
+  g_last_error.clear();
+  if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
+  gemm_status_t st = check_common(M, N, K, dtype, epi, stages);
+  if (st != GEMM_OK) return st;
+  if (M != plan->M || N != plan->N || K != plan->K || dtype != plan->dtype || epi != plan->epi ||
+      stages != plan->stages)
+    return fail(GEMM_ERR_PLAN_MISMATCH, "run arguments differ from the plan");
+  const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
+  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  if (bytesC == 0) return GEMM_OK;
+  if (!hC || (bytesA && !hA) || (bytesB && !hB))
+    return fail(GEMM_ERR_INVALID_ARG, "NULL host buffer");
+  DeviceGuard guard(plan->device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_handle);
+  cudaError_t e;
+  if (!plan->hC) {
+    if (bytesA && (e = cudaMalloc(&plan->hA, bytesA)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(A)");
+    if (bytesB && (e = cudaMalloc(&plan->hB, bytesB)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(B)");
+    if ((e = cudaMalloc(&plan->hC, bytesC)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(C)");
+  }
+  if (bytesA && (e = cudaMemcpyAsync(plan->hA, hA, bytesA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e, "copy A to device");
+  if (bytesB && (e = cudaMemcpyAsync(plan->hB, hB, bytesB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e, "copy B to device");
+  st = gemm_run(plan, plan->hA, plan->hB, plan->hC, M, N, K, dtype, epi, stages, stream_handle);
+  if (st != GEMM_OK) return st;
+  if ((e = cudaMemcpyAsync(hC, plan->hC, bytesC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "copy C to host");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t* detail) {
+  g_last_error.clear();
+  if (!plan || !device_status) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+  DeviceGuard guard(plan->device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  int h[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(h, plan->d_status, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  e = cudaMemset(plan->d_status, 0, sizeof(h));
+  if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  *device_status = h[0];
+  if (detail) *detail = h[1];
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info) {
+  if (!plan || !info) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+  info->tile_m = kBM;
+  info->tile_n = plan->bn;
+  info->tile_k = kBK;
+  info->stages = plan->stages;
+  info->accumulators = plan->num_acc;
+  info->raster_group = plan->raster_group;
+  info->grid = plan->grid;
+  info->num_tiles = plan->num_tiles;
+  info->smem_bytes = plan->smem;
+  info->pads_operands = plan->last_pads;
+  info->tma_store = plan->last_tma_store;
+  info->kernels_per_run = plan->last_kernels;
+  info->sm_count = plan->sm_count;
+  return GEMM_OK;
+}
+
+void gemm_plan_destroy(gemm_plan_t* plan) {
+  if (!plan) return;
+  {
+    DeviceGuard guard(plan->device);
+    if (guard.err == cudaSuccess) {
+      cudaDeviceSynchronize();
+      if (plan->d_status) cudaFree(plan->d_status);
+      if (plan->scratch) cudaFree(plan->scratch);
+      if (plan->hA) cudaFree(plan->hA);
+      if (plan->hB) cudaFree(plan->hB);
+      if (plan->hC) cudaFree(plan->hC);
+    }
+  }
+  delete plan;
+}
+
+}  // extern "C"

@@ -1,0 +1,337 @@
+// gemm_kernel.cuh -- persistent, warp-specialised sm_103a GEMM
+//
+//   C[M,N] = epi(A[M,K] . B[N,K]^T), fp16/bf16 in, fp32 accumulate in TMEM.
+//
+// Structure (TileLang tutorial ch. 11 "pipelined_gemm.py", matmul_auto, for
+// the tile loop; Mosaic GPU pipelining guide, "Warp Specialization", for the
+// split into a memory thread and compute threads):
+//
+//   warp 0  (one lane)  TMA producer: for every tile the CTA owns and every
+//                       64-wide K slice, wait until ring slot s is empty,
+//                       then load the A tile (128 x 64) and B tile (BN x 64)
+//                       into slot s with 128-byte swizzling; the copy engine
+//                       counts the bytes onto full[s].
+//   warp 1  (one lane)  MMA issuer: wait full[s], issue four
+//                       tcgen05.mma (K = 16 each) into the tile's TMEM
+//                       accumulator, then tcgen05.commit -> empty[s].  The
+//                       slot is released only when those MMAs have finished
+//                       reading it (the hazard the guide's delay_release
+//                       covers), and the issuer never waits on its own MMAs.
+//                       After the last K slice: commit -> tmem_full[acc].
+//   warps 2-5           epilogue: wait tmem_full[acc], tcgen05.ld 32 rows x
+//                       64 columns per step, optional tanh-GELU in fp32,
+//                       round to fp16/bf16, write a swizzled staging tile and
+//                       send it out with a TMA store (or masked st.global
+//                       when C's pitch is not 16-byte aligned); then arrive
+//                       on tmem_empty[acc].
+//
+// With two TMEM accumulators the epilogue of tile t overlaps the main loop
+// of tile t+1.  The CTAs are persistent: CTA b walks tiles b, b + grid, ...
+// of a grouped ("rasterised") tile order that keeps `raster_group` tile rows
+// together so concurrently running CTAs share A and B slices in L2.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
+// records GEMM_ERR_TIMEOUT in the status word and its role stops, after which
+// the CTA drains its in-flight copies and MMAs and frees its TMEM.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "kernel_params.h"
+#include "ptx.cuh"
+
+namespace spgemm {
+
+static __device__ __noinline__ void record_error(int* status, int code, int detail) {
+  if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
+}
+
+// Wait for the phase of parity `parity` of barrier `bar`; false on timeout.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p,
+                                             int detail) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      record_error(p.status, kStatusTimeout, detail);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Grouped tile order: tiles are taken `raster_group` tile rows at a time,
+// column by column inside a group.
+__device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
+  const int per_group = p.raster_group * p.tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * p.raster_group;
+  const int rows = min(p.tiles_m - first_m, p.raster_group);
+  const int r = t - g * per_group;
+  mb = first_m + r % rows;
+  nb = r / rows;
+}
+
+__device__ __forceinline__ float gelu_tanh(float x) {
+  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)); this form cannot produce
+  // inf/inf for large |u| (x -> x for u -> +inf, x -> -0 for u -> -inf).
+  const float u = 0.7978845608f * (x + 0.044715f * x * x * x);
+  return x / (1.0f + __expf(-2.0f * u));
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const Params p) {
+  constexpr uint32_t kStageB = BN * kBK * 2;
+  constexpr uint32_t kStage = kStageA + kStageB;
+  constexpr uint32_t kChunks = BN / kStoreCols;
+
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B
+  // and the MMA descriptors assume atoms start on that boundary.
+  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_addr(smem);
+
+  const int S = p.stages;
+  const uint32_t ring_bytes = static_cast<uint32_t>(S) * kStage;
+  uint8_t* staging = smem + ring_bytes;
+  const uint32_t staging_bytes = kEpiWarps * p.store_bufs * kStoreBuf;
+  const uint32_t bar_base = sbase + ring_bytes + staging_bytes;
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
+  auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + a); };
+  auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + 2 + a); };
+  const uint32_t done_bar = bar_base + 8u * (2 * kMaxStages + 4);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 5));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t tmem_cols = static_cast<uint32_t>(p.tmem_cols);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), kEpiWarps);
+    }
+    ptx::mbar_init(done_bar, 1);
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+    if (p.tma_store) ptx::tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per-slot: used at all / parity of last use
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full_bar(stage), kStage);
+          const uint32_t sa = sbase + stage * kStage;
+          ptx::tma_load_2d(sa, &tmA, kb * kBK, mb * kBM, full_bar(stage));
+          ptx::tma_load_2d(sa + kStageA, &tmB, kb * kBK, nb * BN, full_bar(stage));
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every copy this thread started must have landed before the CTA exits.
+      for (int s = 0; s < S; ++s)
+        if (issued & (1u << s))
+          wait_bounded(full_bar(s), (issued_parity >> s) & 1u, p, kDetailProducerDrain);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty)) break;
+        ptx::tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, p, kDetailMmaFull)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint32_t sa = sbase + stage * kStage;
+          const uint64_t a_desc = ptx::smem_desc_k_sw128(sa);
+          const uint64_t b_desc = ptx::smem_desc_k_sw128(sa + kStageA);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+            // descriptor's address field (16-byte units).
+            ptx::mma_f16_ss(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                            (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(tfull_bar(acc));
+        if (++acc == p.num_acc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs this thread issued must be complete before TMEM is freed.
+      ptx::mma_commit(done_bar);
+      wait_bounded(done_bar, 0, p, kDetailMmaDrain);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- epilogue --
+    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int ew = warp - 2;      // owner index of the staging buffers
+    uint8_t* my_stage = staging + ew * p.store_bufs * kStoreBuf;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int buf = 0;
+    const bool bf16 = p.bf16 != 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      int ready = 1;
+      if (lane == 0) ready = wait_bounded(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      if (!ready) break;
+      ptx::tc_fence_after_sync();
+
+      const int row0 = mb * kBM + q * 32;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      if (row0 < p.M) {
+#pragma unroll 1
+        for (uint32_t c = 0; c < kChunks; ++c) {
+          const int col0 = nb * BN + static_cast<int>(c) * kStoreCols;
+          if (col0 >= p.N) break;
+          uint32_t r0[32], r1[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols, r0);
+          ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols + 32, r1);
+          ptx::tmem_wait_ld();
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
+            float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
+            if (p.gelu) {
+              a0 = gelu_tanh(a0);
+              a1 = gelu_tanh(a1);
+              b0 = gelu_tanh(b0);
+              b1 = gelu_tanh(b1);
+            }
+            pk[j] = pack2(a0, a1, bf16);
+            pk[16 + j] = pack2(b0, b1, bf16);
+          }
+          if (p.tma_store) {
+            // The staging buffer about to be written must have been read out
+            // by the store issued store_bufs chunks ago.
+            if (lane == 0) {
+              if (p.store_bufs == 2)
+                ptx::bulk_wait_group_read<1>();
+              else
+                ptx::bulk_wait_group_read<0>();
+            }
+            __syncwarp();
+            uint8_t* sb = my_stage + buf * kStoreBuf;
+            // Row `lane` is 128 B; 16-byte chunk j lands at j ^ (row % 8),
+            // the layout of a 128-byte-swizzled TMA box (bank-conflict free).
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+              *reinterpret_cast<uint4*>(sb + off) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmC, ptx::smem_addr(sb), col0, row0);
+              ptx::bulk_commit_group();
+            }
+            buf = (buf + 1 == p.store_bufs) ? 0 : buf + 1;
+          } else {
+            const int row = row0 + lane;
+            if (row < p.M) {
+              uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
+              const int ncols = min(kStoreCols, p.N - col0);
+#pragma unroll
+              for (int j = 0; j < kStoreCols; ++j) {
+                if (j < ncols)
+                  crow[col0 + j] = static_cast<uint16_t>(pk[j >> 1] >> ((j & 1) * 16));
+              }
+            }
+          }
+        }
+      }
+      // This warp's TMEM reads of accumulator `acc` are complete (wait::ld).
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+      if (++acc == p.num_acc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group_all();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace spgemm

@@ -1,0 +1,60 @@
+// kernel_params.h -- launch parameters and compile-time geometry shared by
+// the host planner (gemm_api.cu) and the device kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace spgemm {
+
+constexpr int kBM = 128;          // CTA tile rows (one TMEM lane per row)
+constexpr int kBK = 64;           // K slice: 64 x 16-bit = one 128-byte swizzle row
+constexpr int kUmmaK = 16;        // K of one tcgen05.mma kind::f16
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kStageA = kBM * kBK * 2;             // 16 KiB
+constexpr int kStoreCols = 64;                          // epilogue step: 64 columns
+constexpr uint32_t kStoreBuf = 32u * kStoreCols * 2u;   // 32 rows x 128 B = 4 KiB
+constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 5) + 16u;
+constexpr uint32_t kAlignSlack = 1024u;
+
+constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
+
+// Where a device-side wait ran out (status word [1]): role << 16 | wait id.
+constexpr int kDetailProducerEmpty = (1 << 16) | 1;
+constexpr int kDetailProducerDrain = (1 << 16) | 2;
+constexpr int kDetailMmaAccEmpty = (2 << 16) | 1;
+constexpr int kDetailMmaFull = (2 << 16) | 2;
+constexpr int kDetailMmaDrain = (2 << 16) | 3;
+constexpr int kDetailEpiFull = (3 << 16) | 1;
+
+struct Params {
+  int M, N;              // output extent
+  int K;                 // reduction length seen by the tensor maps (padded when staged)
+  int tiles_m, tiles_n;
+  int num_tiles;
+  int k_blocks;          // ceil(K / kBK)
+  int stages;            // ring depth, 1..kMaxStages
+  int num_acc;           // TMEM accumulators, 1 or 2
+  int tmem_cols;         // allocated TMEM columns (power of two >= 32)
+  int raster_group;      // tile rows per raster group
+  int store_bufs;        // staging buffers per epilogue warp (1 or 2)
+  int bf16;              // element type: 0 fp16, 1 bf16
+  int gelu;              // epilogue: 0 none, 1 tanh-GELU
+  int tma_store;         // 1: bulk tensor stores of C; 0: masked st.global
+  uint32_t idesc;        // tcgen05.mma instruction descriptor
+  void* C;               // used by the st.global path
+  int64_t ldc;
+  int* status;           // device status word: [0] code, [1] detail
+  unsigned long long timeout_ns;
+};
+
+// Shared memory a CTA needs for a given tile width / ring depth / staging.
+inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs) {
+  const size_t stage = static_cast<size_t>(kStageA) + static_cast<size_t>(bn) * kBK * 2;
+  return kAlignSlack + stage * static_cast<size_t>(stages) +
+         static_cast<size_t>(kEpiWarps) * store_bufs * kStoreBuf + kBarrierBytes;
+}
+
+}  // namespace spgemm

@@ -1,0 +1,30 @@
+// launch.h -- host-side launchers, one per compiled kernel instance.  Each
+// kernel lives in its own translation unit so the library builds in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernel_params.h"
+
+namespace spgemm {
+
+#define SPGEMM_DECLARE_BN(BN)                                                              \
+  cudaError_t gemm_set_smem_bn##BN(size_t smem);                                           \
+  cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,               \
+                                 const CUtensorMap& c, const Params& p, int grid, size_t smem, \
+                                 cudaStream_t stream);
+SPGEMM_DECLARE_BN(64)
+SPGEMM_DECLARE_BN(128)
+SPGEMM_DECLARE_BN(256)
+#undef SPGEMM_DECLARE_BN
+
+// Copy the rows of A (M x K) and/or B (N x K) into zero-padded scratch with
+// row pitch Kp (a multiple of 8 elements, so every row is 16-byte aligned).
+cudaError_t launch_pad_operands(const uint16_t* A, int64_t M, uint16_t* Ap, const uint16_t* B,
+                                int64_t N, uint16_t* Bp, int64_t K, int64_t Kp, int sm_count,
+                                cudaStream_t stream);
+
+}  // namespace spgemm

@@ -1,0 +1,289 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: bit-exact on small-integer inputs (every partial sum is exact in fp32,
+so the result is independent of summation order); otherwise every element
+within 2 ulps of the output type plus 1e-3 and a relative Frobenius error of
+at most 1e-3.  Small shapes are compared in full; the full-size workloads at
+sampled positions (random plus every tile boundary and the ragged edges),
+with every other element checked to be written and finite.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs
+import oracle
+from tests import gpu_util as gu
+from tests import tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import software_pipelined_tiled_gemm_gb300 as sg
+    sg.load_library()
+
+
+def _int_inputs(M, N, K, dtype, seed):
+    lo, hi = (-2, 2) if dtype == "f16" else (-1, 1)
+    return gemm_inputs.custom(M, N, K, dtype=dtype, dist="int", seed=seed, lo=lo, hi=hi)
+
+
+def _assert_bit_exact(A, B, dtype, C):
+    ref = oracle.gemm_nt(A, B, dtype)
+    assert np.all(np.abs(ref) < (2048 if dtype == "f16" else 256))
+    want = oracle.round_to(ref, dtype)
+    got = gu.bits(C)
+    mism = np.argwhere(want != got)
+    assert mism.size == 0, "first mismatch at %s: got %r want %r" % (
+        tuple(mism[0]), oracle.decode(got[tuple(mism[0])], dtype), ref[tuple(mism[0])])
+
+
+# ---------------------------------------------------------- exactness --
+
+def test_small_integer_config_bit_exact():
+    A, B = gemm_inputs.make("gemm_256_f16_int")
+    C, info, canary = gu.run_device(A, B, "f16")
+    assert canary
+    _assert_bit_exact(A, B, "f16", C)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_every_ring_depth_bit_exact_with_persistent_tiles(stages):
+    # 9 K slices so the ring wraps; 16 tiles over 2 CTAs so each CTA walks 8
+    # tiles and both accumulators change hands several times.
+    A, B = _int_inputs(512, 1024, 576, "f16", seed=100 + stages)
+    C, info, canary = gu.run_device(A, B, "f16", stages=stages, max_ctas=2)
+    assert canary and info["grid"] == 2 and info["stages"] == stages
+    _assert_bit_exact(A, B, "f16", C)
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_each_tile_width_bit_exact(tile_n):
+    A, B = _int_inputs(384, 640, 320, "f16", seed=7)
+    C, info, canary = gu.run_device(A, B, "f16", tile_n=tile_n, max_ctas=3)
+    assert canary and info["tile_n"] == tile_n
+    _assert_bit_exact(A, B, "f16", C)
+
+
+def test_bf16_integer_bit_exact():
+    A, B = _int_inputs(256, 512, 256, "bf16", seed=9)
+    C, _, canary = gu.run_device(A, B, "bf16")
+    assert canary
+    _assert_bit_exact(A, B, "bf16", C)
+
+
+def test_single_buffer_variant_bit_exact():
+    A, B = _int_inputs(384, 512, 640, "f16", seed=11)
+    C, info, canary = gu.run_device(A, B, "f16", stages=1, variant="single_buffer", max_ctas=4)
+    assert canary and info["accumulators"] == 1 and info["stages"] == 1
+    _assert_bit_exact(A, B, "f16", C)
+
+
+def test_repeated_runs_identical_bits():
+    A, B = gemm_inputs.custom(512, 768, 1024, dist="normal_scaled", seed=12)
+    C1, _, _ = gu.run_device(A, B, "f16")
+    C2, _, _ = gu.run_device(A, B, "f16")
+    assert torch.equal(C1.view(torch.int16), C2.view(torch.int16))
+
+
+# ------------------------------------------------------- small configs --
+
+def test_config_256_uniform_f16():
+    A, B = gemm_inputs.make("gemm_256_f16")
+    C, _, canary = gu.run_device(A, B, "f16")
+    st, _, _ = gu.check_full(A, B, "f16", C)
+    assert canary and st["ok"], st
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1), (1, 8, 8), (7, 3, 5), (63, 65, 64), (64, 64, 64), (65, 63, 72), (127, 129, 136),
+    (128, 256, 64), (129, 257, 128), (200, 300, 520), (257, 513, 1000), (300, 200, 8),
+    (1, 1024, 4096), (1000, 1, 64), (333, 999, 77),
+])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_edge_shapes(shape, dtype):
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, dtype=dtype, seed=M * 7 + N * 3 + K)
+    C, info, canary = gu.run_device(A, B, dtype)
+    st, _, _ = gu.check_full(A, B, dtype, C)
+    assert canary, "wrote outside C"
+    assert st["ok"], (shape, st, info)
+    assert info["pads_operands"] == (1 if K % 8 else 0)
+    assert info["tma_store"] == (0 if N % 8 else 1)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 4])
+def test_gelu_bf16_small(stages):
+    A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=192, N=640, K=512)
+    C, _, canary = gu.run_device(A, B, "bf16", epilogue="gelu", stages=stages)
+    st, _, _ = gu.check_full(A, B, "bf16", C, epilogue="gelu")
+    assert canary and st["ok"], st
+
+
+def test_gelu_extreme_values_no_nan():
+    # Large |x| must give x (positive) or -0/tiny (negative), never NaN.
+    K = 64
+    A = torch.zeros(128, K, dtype=torch.bfloat16)
+    B = torch.zeros(256, K, dtype=torch.bfloat16)
+    A[:, 0] = torch.linspace(-300, 300, 128).to(torch.bfloat16)
+    B[:, 0] = torch.linspace(-2, 2, 256).to(torch.bfloat16)
+    C, _, _ = gu.run_device(A, B, "bf16", epilogue="gelu")
+    assert torch.isfinite(C.float()).all()
+    st, _, _ = gu.check_full(A, B, "bf16", C, epilogue="gelu")
+    assert st["ok"], st
+
+
+def test_gelu_f16():
+    A, B = gemm_inputs.custom(256, 384, 256, dtype="f16", dist="normal_scaled", seed=5)
+    C, _, _ = gu.run_device(A, B, "f16", epilogue="gelu")
+    st, _, _ = gu.check_full(A, B, "f16", C, epilogue="gelu")
+    assert st["ok"], st
+
+
+# ------------------------------------------------ alignment / fallbacks --
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 3, 0), (0, 0, 1), (8, 8, 8), (5, 7, 3)])
+def test_unaligned_base_addresses(offsets):
+    a_off, b_off, c_off = offsets
+    A, B = gemm_inputs.custom(200, 264, 192, seed=sum(offsets))
+    C, info, canary = gu.run_device(A, B, "f16", a_offset=a_off, b_offset=b_off, c_offset=c_off)
+    st, _, _ = gu.check_full(A, B, "f16", C)
+    assert canary and st["ok"], (offsets, st)
+    assert info["pads_operands"] == (1 if (a_off % 8 or b_off % 8) else 0)
+    assert info["tma_store"] == (0 if c_off % 8 else 1)
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A = torch.zeros(100, 0, dtype=torch.float16)
+    B = torch.zeros(70, 0, dtype=torch.float16)
+    C, info, canary = gu.run_device(A, B, "f16", epilogue="gelu")
+    assert canary and (C.view(torch.int16) == 0).all() and info["kernels_per_run"] == 0
+    for M, N in ((0, 5), (5, 0)):
+        plan = sg.Plan(M, N, 16, "f16")
+        c = torch.empty(max(M * N, 1), dtype=torch.float16, device="cuda")
+        a = torch.empty(max(M * 16, 1), dtype=torch.float16, device="cuda")
+        b = torch.empty(max(N * 16, 1), dtype=torch.float16, device="cuda")
+        plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), 0)
+        plan.close()
+
+
+def test_plan_mismatch_and_aliasing_rejected():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    plan = sg.Plan(128, 128, 64, "f16")
+    a = torch.zeros(128 * 64, dtype=torch.float16, device="cuda")
+    c = torch.zeros(128 * 128, dtype=torch.float16, device="cuda")
+    st = sg.gemm_run(plan.handle, a.data_ptr(), a.data_ptr(), c.data_ptr(), 128, 128, 32, 0, 0, 4, 0)
+    assert st == sg.GEMM_ERR_PLAN_MISMATCH
+    st = sg.gemm_run(plan.handle, a.data_ptr(), a.data_ptr(), c.data_ptr(), 128, 128, 64, 1, 0, 4, 0)
+    assert st == sg.GEMM_ERR_PLAN_MISMATCH
+    st = sg.gemm_run(plan.handle, c.data_ptr(), a.data_ptr(), c.data_ptr(), 128, 128, 64, 0, 0, 4, 0)
+    assert st == sg.GEMM_ERR_INVALID_ARG
+    st = sg.gemm_run(plan.handle, a.data_ptr() + 1, a.data_ptr(), c.data_ptr(), 128, 128, 64, 0, 0, 4, 0)
+    assert st == sg.GEMM_ERR_INVALID_ARG      # odd address
+    plan.close()
+
+
+def test_smem_budget_reported_not_clamped():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    with pytest.raises(sg.GemmError) as ei:
+        sg.Plan(4096, 4096, 4096, "f16", stages=5, tile_n=256)
+    assert ei.value.status == sg.GEMM_ERR_SMEM_BUDGET
+    p = sg.Plan(4096, 4096, 4096, "f16", stages=6)      # auto: narrower tile fits
+    assert p.info()["stages"] == 6 and p.info()["tile_n"] < 256
+    p.close()
+
+
+def test_run_host_end_to_end():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = gemm_inputs.custom(300, 520, 264, seed=21)
+    C = torch.empty(300, 520, dtype=torch.float16).pin_memory()
+    Ap, Bp = A.pin_memory(), B.pin_memory()
+    plan = sg.Plan(300, 520, 264, "f16")
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        C.zero_()
+        plan.run_host(Ap.data_ptr(), Bp.data_ptr(), C.data_ptr(), stream.cuda_stream)
+        st, _, _ = gu.check_full(A, B, "f16", C)
+        assert st["ok"], st
+    plan.close()
+
+
+def test_matmul_nt_torch_layer_on_current_stream():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = gemm_inputs.custom(256, 512, 320, dtype="bf16", seed=22)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        C = sg.matmul_nt(A.cuda(), B.cuda(), epilogue="gelu", stages=3)
+    s.synchronize()
+    st, _, _ = gu.check_full(A, B, "bf16", C.cpu(), epilogue="gelu")
+    assert st["ok"], st
+
+
+# ---------------------------------------------- full-size workloads --
+
+def _full_size(name, stages=4, variant="pipelined", count=3000, **tuning):
+    w = gemm_inputs.WORKLOADS[name]
+    A, B = gemm_inputs.make(w)
+    C, info, canary = gu.run_device(A, B, w.dtype, epilogue=None if w.epilogue == "none" else "gelu",
+                                    stages=stages, variant=variant, **tuning)
+    assert canary
+    assert torch.isfinite(C.float()).all(), "unwritten (NaN-filled) or non-finite outputs"
+    r, c = gu.sample_positions(w.M, w.N, count, seed=w.seed, tile_n=info["tile_n"])
+    st = gu.check_sampled(A, B, w.dtype, C, r, c,
+                          epilogue=None if w.epilogue == "none" else "gelu")
+    assert st["ok"], (name, st, info)
+    return A, B, C, info
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4, 5, 6])
+def test_config_4096_stage_sweep(stages):
+    _full_size("gemm_4096_f16", stages=stages)
+
+
+def test_config_8192_pipelined():
+    A, B, C, info = _full_size("gemm_8192_f16", stages=4)
+    # Row-sum property over every output: sum_j C[i,j] ~= a_i . (sum_j b_j)
+    a = A.double().cuda()
+    bs = B.double().cuda().sum(0)
+    want = (a @ bs).cpu()
+    got = C.cuda().double().sum(1).cpu()
+    # each C element carries <= 2 ulp(fp16) rounding; 8192 of them per row
+    assert torch.max(torch.abs(got - want)).item() < 8192 * 2 ** -11 * 0.05 + 1e-3
+
+
+def test_config_8192_single_buffer():
+    _full_size("gemm_8192_f16", stages=1, variant="single_buffer", count=1500)
+
+
+def test_config_gelu_layer_bf16():
+    _full_size("gelu_3072x16384x4096_bf16", stages=4)
+
+
+def test_config_ragged():
+    A, B, C, info = _full_size("ragged_4095x4097x8191_f16", stages=4)
+    assert info["pads_operands"] == 1 and info["tma_store"] == 0
+    # the whole last row and last column (partial tiles on every dimension)
+    M, N = 4095, 4097
+    r = np.concatenate([np.full(N, M - 1), np.arange(M)])
+    c = np.concatenate([np.arange(N), np.full(M, N - 1)])
+    st = gu.check_sampled(A, B, "f16", C, r, c)
+    assert st["ok"], st
+
+
+def test_config_skinny():
+    _full_size("skinny_64x8192x8192_f16", stages=4)
+
+
+def test_mosaic_guide_shape_full_compare():
+    w = gemm_inputs.WORKLOADS["mosaic_16896x512x640_f16"]
+    A, B = gemm_inputs.make(w)
+    C, _, canary = gu.run_device(A, B, "f16")
+    st, _, _ = gu.check_full(A, B, "f16", C)
+    assert canary and st["ok"], st
