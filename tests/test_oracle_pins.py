@@ -309,3 +309,18 @@ def test_ulp_definition_matches_numpy_spacing():
     x16 = x16[x16 > 0]
     assert np.array_equal(tolerance.ulp(x16.astype(np.float64), "f16"),
                           np.spacing(x16).astype(np.float64))
+
+
+def test_bf16_rounding_floor_exceeds_frobenius_bound():
+    # The reason the bf16 Frobenius check is taken against the correctly rounded
+    # result: rounding alone already costs more than 1e-3 relative.
+    A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=128, N=256, K=256)
+    ref = oracle.gemm_nt(A, B, "bf16", epilogue="gelu")
+    rnd = oracle.decode(oracle.round_to(ref, "bf16"), "bf16")
+    assert np.linalg.norm(rnd - ref) / np.linalg.norm(ref) > 1e-3
+    st = tolerance.compare(rnd, ref, "bf16")
+    assert st["ok"] and st["frob"] == 0.0
+    # one element off by 3 ulps still fails per element
+    bad = rnd.copy()
+    bad[5, 7] += 3 * tolerance.ulp(ref[5, 7], "bf16") + 1.001e-3
+    assert not tolerance.compare(bad, ref, "bf16")["ok"]

@@ -5,6 +5,14 @@ absolute 1e-3, and a relative Frobenius error of at most 1e-3.  The ulp is
 the spacing of the output format in the binade of |ref|:
   fp16:  2^(floor(log2|x|) - 10) for |x| >= 2^-14, else 2^-24;
   bf16:  2^(floor(log2|x|) - 7)  for |x| >= 2^-126, else 2^-133.
+
+Reading of the Frobenius bound for bf16: rounding the exact result once to
+bf16 (8 significant bits) already leaves a relative Frobenius error of about
+1.6e-3, above the 1e-3 bound, so no bf16 output can meet it literally.  For
+bf16 the Frobenius error is therefore measured against the oracle's result
+correctly rounded to bf16 (the error the computation adds beyond the one
+unavoidable output rounding); fp16 is checked literally against the exact
+result.
 """
 from __future__ import annotations
 
@@ -27,6 +35,11 @@ def ulp(x, dtype: str) -> np.ndarray:
     return np.ldexp(1.0, q)
 
 
+def rounded_reference(ref, dtype: str) -> np.ndarray:
+    import oracle
+    return oracle.decode(oracle.round_to(ref, dtype), dtype)
+
+
 def compare(got, ref, dtype: str, ulps: float = ULPS, abs_tol: float = ABS):
     """Return a dict of error statistics; `ok` is the pass/fail verdict."""
     g = np.asarray(got, dtype=np.float64)
@@ -40,10 +53,13 @@ def compare(got, ref, dtype: str, ulps: float = ULPS, abs_tol: float = ABS):
     finite = np.isfinite(g)
     bad = (~finite) | (err > bound)
     nr = np.linalg.norm(r)
-    frob = float(np.linalg.norm(np.where(finite, g - r, np.inf)) / nr) if nr > 0 else float(
-        np.linalg.norm(g - r))
+    frob_base = r if dtype == "f16" else rounded_reference(r, dtype)
+    diff = np.where(finite, g - frob_base, np.inf)
+    frob = float(np.linalg.norm(diff) / nr) if nr > 0 else float(np.linalg.norm(diff))
+    frob_exact = float(np.linalg.norm(np.where(finite, g - r, np.inf)) / nr) if nr > 0 else 0.0
     return {
         "ok": bool((not bad.any()) and frob <= FROB),
+        "frob_vs_exact": frob_exact,
         "max_abs": float(np.max(np.where(finite, err, np.inf))),
         "max_ulp": float(np.max(np.where(finite, err / u, np.inf))),
         "frob": frob,
