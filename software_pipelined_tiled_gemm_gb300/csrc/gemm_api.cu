@@ -321,7 +321,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   if (want_ctas > 0) cap = std::min(cap, want_ctas);
   p->grid = static_cast<int>(std::min<int64_t>(p->num_tiles, cap));
 
-  e = set_smem(p->bn, p->smem);
+  // The limit is per kernel function, shared by every plan on the device:
+  // always raise it to the device maximum, never to this plan's own size, so
+  // a later plan with a smaller ring cannot lower it under an earlier one.
+  e = set_smem(p->bn, static_cast<size_t>(smem_optin));
   if (e != cudaSuccess) {
     delete p;
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");

@@ -287,3 +287,20 @@ def test_mosaic_guide_shape_full_compare():
     C, _, canary = gu.run_device(A, B, "f16")
     st, _, _ = gu.check_full(A, B, "f16", C)
     assert canary and st["ok"], st
+
+
+def test_plans_with_different_rings_coexist():
+    # Creating a plan with a small ring after one with a large ring must not
+    # break the large one (the shared-memory limit is per kernel function).
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = _int_inputs(256, 512, 256, "f16", seed=31)
+    big = sg.Plan(256, 512, 256, "f16", stages=4, tile_n=256)
+    small = sg.Plan(256, 512, 256, "f16", stages=1, tile_n=256)
+    a, b = A.cuda(), B.cuda()
+    for plan in (big, small, big):
+        c = torch.full((256, 512), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+        _assert_bit_exact(A, B, "f16", c.cpu())
+    big.close()
+    small.close()
