@@ -81,7 +81,7 @@ def load_peaks():
 
 def source_digest():
     from software_pipelined_tiled_gemm_gb300 import _build
-    return _build._digest()
+    return _build.kernel_digest()
 
 
 def traffic_from_profiles(workload, digest):

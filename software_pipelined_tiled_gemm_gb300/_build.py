@@ -23,7 +23,8 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libspgemm.so")
 STAMP = os.path.join(LIBDIR, "libspgemm.stamp")
 
-SOURCES = ["gemm_api.cu", "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu", "pad.cu"]
+SOURCES = ["gemm_api.cu", "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu", "pad.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
@@ -47,6 +48,22 @@ def _digest() -> str:
         h.update(fh.read())
     h.update(" ".join(ARCH + FLAGS).encode())
     return h.hexdigest()
+
+
+KERNEL_FILES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "gemm_instance.cuh",
+                "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu"]
+
+
+def kernel_digest() -> str:
+    """Content hash of the GEMM kernel's device code only (what an ncu capture
+    of the kernel depends on), independent of the host planner."""
+    h = hashlib.sha256()
+    for f in KERNEL_FILES:
+        h.update(f.encode())
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS).encode())
+    return h.hexdigest()[:16]
 
 
 def up_to_date() -> bool:
