@@ -175,6 +175,43 @@ size_t gemm_smem_bytes(int bm, int bn, int bk, int elem_bytes, int stages);
 /* Library version as "major.minor.patch". */
 const char* gemm_version(void);
 
+/* ---- Allocation-free entry point --------------------------------------------
+ * None of the pages has a counterpart to this call; it exists for users of
+ * the library, not for the method.
+ *
+ * For callers that cannot allocate device memory (no cudaMalloc, no
+ * allocating library routine): code running under an allocator it does not
+ * control, a runtime that forbids allocations once it has started, or a
+ * caller that must not add allocations while other GPU work is being set
+ * up.  gemm_run needs a plan, and a plan allocates its status word and,
+ * for operands whose row pitch or base address is not 16-byte aligned,
+ * scratch for padded copies.  gemm_run_noalloc takes no plan and allocates
+ * nothing: its scratch is one static device array of
+ * GEMM_NOALLOC_SCRATCH_BYTES (plus 256 bytes of status words) that every
+ * GPU loading this library reserves until the process exits.
+ *
+ * Arguments: as gemm_run, without the plan; A, B, C are device pointers on
+ * the current device, `stream` a cudaStream_t (NULL = legacy stream).
+ * Asynchronous.  Returns GEMM_ERR_INVALID_ARG when the padded copies would
+ * need more than GEMM_NOALLOC_SCRATCH_BYTES (that is, when
+ * ((A misaligned or K % 8 ? M : 0) + (B misaligned or K % 8 ? N : 0)) *
+ * round_up(K, 8) * 2 exceeds it); aligned problems need no scratch and have
+ * no such limit.  Device-side wait timeouts are recorded in the static
+ * status word but not reported (there is no plan to read them from).
+ *
+ * The first call on each device sets that device up (takes the device
+ * address of the static array with cudaGetSymbolAddress, sets the kernels'
+ * shared-memory limits, looks up the tensor-map encoder).  Make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array and leaves its contents behind (the status words are cleared at the
+ * start of each call): calls whose work overlaps on the GPU -- on different
+ * streams, or from different host threads -- race on it. */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                               int64_t K, gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

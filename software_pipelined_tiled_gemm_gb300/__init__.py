@@ -27,7 +27,7 @@ __all__ = [
     "GemmError", "Plan", "matmul_nt", "load_library", "library_path",
     "gemm_plan_create", "gemm_plan_create_ex", "gemm_run", "gemm_run_host", "gemm_plan_check",
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
-    "gemm_last_error", "gemm_version", "GemmTuning", "GemmPlanInfo",
+    "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
     "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
     "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH",
@@ -125,6 +125,8 @@ def load_library(path: Optional[str] = None):
         lib.gemm_smem_bytes.restype = ctypes.c_size_t
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = ctypes.c_char_p
+        lib.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
+        lib.gemm_run_noalloc.restype = ci
         _lib = lib
         return lib
 
@@ -182,6 +184,11 @@ def gemm_run(plan, A, B, C, M, N, K, dtype, epi, stages, stream):
 
 def gemm_run_host(plan, hA, hB, hC, M, N, K, dtype, epi, stages, stream):
     return load_library().gemm_run_host(plan, hA, hB, hC, M, N, K, dtype, epi, stages, stream)
+
+
+def gemm_run_noalloc(A, B, C, M, N, K, dtype, epi, stages, stream):
+    """Allocation-free GEMM (no plan); see include/gemm.h.  Returns the status."""
+    return load_library().gemm_run_noalloc(A, B, C, M, N, K, dtype, epi, stages, stream)
 
 
 def gemm_plan_check(plan):
