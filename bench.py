@@ -46,14 +46,15 @@ def log(*a):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_8192_f16", choices=sorted(gemm_inputs.WORKLOADS))
-    ap.add_argument("--stages", type=int, default=4)
+    ap.add_argument("--stages", type=int, default=6)
     ap.add_argument("--variant", default="pipelined", choices=["pipelined", "single_buffer"])
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
+    ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -123,7 +124,7 @@ class ClockSampler:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -249,7 +250,7 @@ def main():
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
     plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
-                   tile_n=args.tile_n, raster_group=args.raster_group)
+                   tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group)
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
     a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
@@ -301,7 +302,8 @@ def main():
         hA, hB = A_cpu.pin_memory(), B_cpu.pin_memory()
         hC = torch.empty(w.M, w.N, dtype=A_cpu.dtype).pin_memory()
         eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
-                        tile_n=args.tile_n, raster_group=args.raster_group)
+                        tile_n=args.tile_n, raster_group=args.raster_group,
+                        cta_group=args.cta_group)
         eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
         barrier()
         t0 = time.perf_counter()
@@ -356,6 +358,7 @@ def main():
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],
+                "cta_group": info["cta_group"],
                 "l2": ("inputs larger than L2 (%d MiB of operands vs %d MiB L2); no flush"
                        % ((w.M * w.K + w.N * w.K) * 2 >> 20, L2_BYTES >> 20))
                 if (w.M * w.K + w.N * w.K) * 2 > L2_BYTES else "operands fit in L2 (warm)",

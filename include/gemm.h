@@ -89,9 +89,12 @@ typedef struct gemm_plan gemm_plan_t; /* opaque */
 
 /* Optional tuning knobs for gemm_plan_create_ex.  Zero means "choose". */
 typedef struct {
-  int tile_n;          /* output tile width: 0 (auto), 64, 128 or 256; tile height is 128 */
+  int tile_n;          /* output tile width: 0 (auto), 64, 128 or 256 */
   int raster_group;    /* tile rows walked together for L2 reuse; 0 = auto */
   int max_ctas;        /* cap on persistent CTAs; 0 = one per SM */
+  int cta_group;       /* CTAs per output tile: 0 (auto), 1 (128-row tiles), or 2
+                          (a CTA pair on two SMs computes a 256-row tile with
+                          cta_group::2 MMAs; tile_n then 128 or 256) */
   int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
 } gemm_tuning_t;
 
@@ -108,6 +111,7 @@ typedef struct {
   int tma_store;               /* last run stored C with bulk tensor stores */
   int kernels_per_run;         /* kernel launches of the last run */
   int sm_count;
+  int cta_group;               /* CTAs per output tile (1 or 2) */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

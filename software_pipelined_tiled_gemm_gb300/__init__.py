@@ -55,7 +55,8 @@ GEMM_SINGLE_BUFFER = 1
 
 class GemmTuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
-                ("max_ctas", ctypes.c_int), ("timeout_ns", ctypes.c_int64)]
+                ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
+                ("timeout_ns", ctypes.c_int64)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -64,7 +65,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("raster_group", ctypes.c_int), ("grid", ctypes.c_int),
                 ("num_tiles", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t),
                 ("pads_operands", ctypes.c_int), ("tma_store", ctypes.c_int),
-                ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int)]
+                ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int),
+                ("cta_group", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -229,7 +231,7 @@ class Plan:
     """Owns one gemm_plan_t."""
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
-                 tile_n=0, raster_group=0, max_ctas=0, timeout_ns=0):
+                 tile_n=0, raster_group=0, max_ctas=0, cta_group=0, timeout_ns=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -237,7 +239,8 @@ class Plan:
         self.variant = _VAR[variant] if isinstance(variant, str) else int(variant)
         self.device = int(device)
         self._h = None
-        tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(timeout_ns))
+        tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
+                            int(timeout_ns))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")

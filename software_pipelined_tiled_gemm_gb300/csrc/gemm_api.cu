@@ -99,6 +99,7 @@ struct gemm_plan {
   gemm_variant_t variant = GEMM_PIPELINED;
 
   int sm_count = 0;
+  int cg = 1;                    // CTAs per output tile (2 = CTA pair)
   int bn = 256;
   int num_acc = 2;
   int store_bufs = 2;
@@ -170,7 +171,8 @@ gemm_status_t check_common(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-cudaError_t set_smem(int bn, size_t smem) {
+cudaError_t set_smem(int bn, int cg, size_t smem) {
+  if (cg == 2) return bn == 128 ? gemm_set_smem_pair128(smem) : gemm_set_smem_pair256(smem);
   switch (bn) {
     case 64: return gemm_set_smem_bn64(smem);
     case 128: return gemm_set_smem_bn128(smem);
@@ -178,8 +180,11 @@ cudaError_t set_smem(int bn, size_t smem) {
   }
 }
 
-cudaError_t launch(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                   const Params& p, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch(int bn, int cg, const CUtensorMap& a, const CUtensorMap& b,
+                   const CUtensorMap& c, const Params& p, int grid, size_t smem, cudaStream_t s) {
+  if (cg == 2)
+    return bn == 128 ? gemm_launch_pair128(a, b, c, p, grid, smem, s)
+                     : gemm_launch_pair256(a, b, c, p, grid, smem, s);
   switch (bn) {
     case 64: return gemm_launch_bn64(a, b, c, p, grid, smem, s);
     case 128: return gemm_launch_bn128(a, b, c, p, grid, smem, s);
@@ -230,14 +235,19 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     return fail(GEMM_ERR_INVALID_ARG, "the single-buffer variant has exactly 1 stage (got %d)",
                 stages);
   if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
-  int want_bn = 0, want_group = 0, want_ctas = 0;
+  int want_bn = 0, want_group = 0, want_ctas = 0, want_cg = 0;
   unsigned long long timeout = kDefaultTimeoutNs;
   if (tuning) {
     want_bn = tuning->tile_n;
     want_group = tuning->raster_group;
     want_ctas = tuning->max_ctas;
+    want_cg = tuning->cta_group;
     if (want_bn != 0 && want_bn != 64 && want_bn != 128 && want_bn != 256)
       return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", want_bn);
+    if (want_cg < 0 || want_cg > 2)
+      return fail(GEMM_ERR_INVALID_ARG, "cta_group %d not in {0, 1, 2}", want_cg);
+    if (want_cg == 2 && want_bn == 64)
+      return fail(GEMM_ERR_INVALID_ARG, "CTA pairs use tile_n 128 or 256");
     if (want_group < 0 || want_ctas < 0)
       return fail(GEMM_ERR_INVALID_ARG, "negative raster_group / max_ctas");
     if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
@@ -260,6 +270,55 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem optin)");
 
+  // Tile shape.  Candidates in order of preference: CTA pairs (256-row
+  // tiles; each CTA holds half of B, so a slot is 32 KiB at tile_n 256 and
+  // deeper rings fit) when at least one full wave of pair tiles exists,
+  // then single-CTA 128-row tiles from the widest down.  A candidate must
+  // fit the shared-memory budget; single-CTA widths narrow while the widest
+  // leaves most SMs idle (fewer tiles than SMs).
+  struct Cand { int cg, bn; };
+  const Cand cands[5] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
+  int chosen = 0, chosen_cg = 1, chosen_bufs = 0, chosen_clusters = 0;
+  size_t chosen_smem = 0;
+  for (int i = 0; i < 5; ++i) {
+    const int cg = cands[i].cg, bn = cands[i].bn;
+    if (want_bn != 0 && bn != want_bn) continue;
+    if (want_cg != 0 && cg != want_cg) continue;
+    int bufs = 2;
+    size_t need = kernel_smem_bytes(bn, stages, bufs, cg);
+    if (need > static_cast<size_t>(smem_optin)) {
+      bufs = 1;
+      need = kernel_smem_bytes(bn, stages, bufs, cg);
+    }
+    if (need > static_cast<size_t>(smem_optin)) continue;
+    const int64_t tiles =
+        cdiv(std::max<int64_t>(M, 1), kBM * cg) * cdiv(std::max<int64_t>(N, 1), bn);
+    int clusters = 0;
+    if (cg == 2) {
+      // Auto mode takes pairs only for problems with at least a wave of pair tiles.
+      if (want_cg == 0 && M <= kBM) continue;
+      e = set_smem(bn, cg, static_cast<size_t>(smem_optin));
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      e = bn == 128 ? gemm_max_clusters_pair128(need, &clusters)
+                    : gemm_max_clusters_pair256(need, &clusters);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+      if (clusters < 1) continue;
+      if (want_cg == 0 && tiles < clusters) continue;
+    }
+    chosen = bn;
+    chosen_cg = cg;
+    chosen_smem = need;
+    chosen_bufs = bufs;
+    chosen_clusters = clusters;
+    if (want_bn != 0 || cg == 2 || tiles >= prop.multiProcessorCount) break;
+  }
+  if (chosen == 0) {
+    return fail(GEMM_ERR_SMEM_BUDGET,
+                "stages=%d does not fit %d B of shared memory at tile width %d (ring %zu B)",
+                stages, smem_optin, want_bn ? want_bn : 64,
+                gemm_smem_bytes(kBM, want_bn ? want_bn : 64, kBK, 2, stages));
+  }
+
   gemm_plan* p = new (std::nothrow) gemm_plan();
   if (!p) return fail(GEMM_ERR_INVALID_ARG, "out of host memory");
   p->device = device;
@@ -274,57 +333,34 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->timeout_ns = timeout;
   p->num_acc = variant == GEMM_SINGLE_BUFFER ? 1 : 2;
   p->max_ctas = want_ctas;
-
-  // Tile width: explicit, or the widest that fits the budget, narrowed while
-  // the widest leaves most SMs idle (fewer tiles than SMs).
-  const int cands[3] = {256, 128, 64};
-  int chosen = 0;
-  size_t chosen_smem = 0;
-  int chosen_bufs = 0;
-  const int64_t tm = cdiv(std::max<int64_t>(M, 1), kBM);
-  for (int i = 0; i < 3; ++i) {
-    const int bn = cands[i];
-    if (want_bn != 0 && bn != want_bn) continue;
-    int bufs = 2;
-    size_t need = kernel_smem_bytes(bn, stages, bufs);
-    if (need > static_cast<size_t>(smem_optin)) {
-      bufs = 1;
-      need = kernel_smem_bytes(bn, stages, bufs);
-    }
-    if (need > static_cast<size_t>(smem_optin)) continue;
-    const int64_t tiles = tm * cdiv(std::max<int64_t>(N, 1), bn);
-    chosen = bn;
-    chosen_smem = need;
-    chosen_bufs = bufs;
-    if (want_bn != 0 || tiles >= p->sm_count) break;
-  }
-  if (chosen == 0) {
-    delete p;
-    return fail(GEMM_ERR_SMEM_BUDGET,
-                "stages=%d does not fit %d B of shared memory at tile width %d (ring %zu B)",
-                stages, smem_optin, want_bn ? want_bn : 64,
-                gemm_smem_bytes(kBM, want_bn ? want_bn : 64, kBK, 2, stages));
-  }
   p->bn = chosen;
+  p->cg = chosen_cg;
   p->smem = chosen_smem;
   p->store_bufs = chosen_bufs;
-  p->tiles_m = cdiv(M, kBM);
+  p->tiles_m = cdiv(M, kBM * chosen_cg);
   p->tiles_n = cdiv(N, chosen);
   p->num_tiles = p->tiles_m * p->tiles_n;
   if (p->num_tiles > kMaxDim) {
     delete p;
     return fail(GEMM_ERR_INVALID_ARG, "too many output tiles");
   }
-  p->raster_group = want_group > 0 ? want_group : 16;
-  if (p->tiles_m > 0) p->raster_group = static_cast<int>(std::min<int64_t>(p->raster_group, p->tiles_m));
-  int cap = p->sm_count;
-  if (want_ctas > 0) cap = std::min(cap, want_ctas);
-  p->grid = static_cast<int>(std::min<int64_t>(p->num_tiles, cap));
+  p->raster_group = want_group > 0 ? want_group : (chosen_cg == 2 ? 8 : 16);
+  if (p->tiles_m > 0)
+    p->raster_group = static_cast<int>(std::min<int64_t>(p->raster_group, p->tiles_m));
+  if (chosen_cg == 2) {
+    int clusters = chosen_clusters;
+    if (want_ctas > 0) clusters = std::min(clusters, std::max(1, want_ctas / 2));
+    p->grid = 2 * static_cast<int>(std::min<int64_t>(p->num_tiles, clusters));
+  } else {
+    int cap = p->sm_count;
+    if (want_ctas > 0) cap = std::min(cap, want_ctas);
+    p->grid = static_cast<int>(std::min<int64_t>(p->num_tiles, cap));
+  }
 
   // The limit is per kernel function, shared by every plan on the device:
   // always raise it to the device maximum, never to this plan's own size, so
   // a later plan with a smaller ring cannot lower it under an earlier one.
-  e = set_smem(p->bn, static_cast<size_t>(smem_optin));
+  e = set_smem(p->bn, p->cg, static_cast<size_t>(smem_optin));
   if (e != cudaSuccess) {
     delete p;
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
@@ -434,7 +470,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   }
   if (plan->mapB_ptr != effB || plan->mapK != Keff) {
     st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
-                   static_cast<uint32_t>(plan->bn), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                   static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (st != GEMM_OK) return st;
     plan->mapB_ptr = effB;
   }
@@ -466,14 +502,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.bf16 = plan->dtype == GEMM_BF16 ? 1 : 0;
   prm.gelu = plan->epi == GEMM_EPI_GELU_TANH ? 1 : 0;
   prm.tma_store = tma_store ? 1 : 0;
-  prm.idesc = ptx::instr_desc_f16(kBM, plan->bn, plan->dtype == GEMM_BF16);
+  prm.idesc = ptx::instr_desc_f16(kBM * plan->cg, plan->bn, plan->dtype == GEMM_BF16);
   prm.C = C;
   prm.ldc = N;
   prm.status = plan->d_status;
   prm.timeout_ns = plan->timeout_ns;
 
-  cudaError_t e = launch(plan->bn, plan->tmA, plan->tmB, plan->tmC, prm, plan->grid, plan->smem,
-                         stream);
+  cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmC, prm, plan->grid,
+                         plan->smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
   ++kernels;
   plan->last_pads = (padA || padB) ? 1 : 0;
@@ -537,7 +573,7 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
 
 gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info) {
   if (!plan || !info) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
-  info->tile_m = kBM;
+  info->tile_m = kBM * plan->cg;
   info->tile_n = plan->bn;
   info->tile_k = kBK;
   info->stages = plan->stages;
@@ -550,6 +586,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->tma_store = plan->last_tma_store;
   info->kernels_per_run = plan->last_kernels;
   info->sm_count = plan->sm_count;
+  info->cta_group = plan->cg;
   return GEMM_OK;
 }
 

@@ -7,13 +7,50 @@
 #define SPGEMM_DEFINE_BN(BN)                                                                   \
   namespace spgemm {                                                                           \
   cudaError_t gemm_set_smem_bn##BN(size_t smem) {                                              \
-    return cudaFuncSetAttribute(gemm_tn_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                 static_cast<int>(smem));                                       \
   }                                                                                            \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,                   \
                                  const CUtensorMap& c, const Params& p, int grid, size_t smem, \
                                  cudaStream_t stream) {                                        \
-    gemm_tn_kernel<BN><<<grid, kThreads, smem, stream>>>(a, b, c, p);                          \
+    gemm_tn_kernel<BN, 1><<<grid, kThreads, smem, stream>>>(a, b, c, p);                          \
     return cudaGetLastError();                                                                 \
   }                                                                                            \
+  }
+
+#define SPGEMM_DEFINE_PAIR(BN)                                                                  \
+  namespace spgemm {                                                                            \
+  cudaError_t gemm_set_smem_pair##BN(size_t smem) {                                             \
+    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 2>,                                          \
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,                    \
+                                static_cast<int>(smem));                                        \
+  }                                                                                             \
+  static void pair_config_##BN(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int grid,    \
+                               size_t smem, cudaStream_t stream) {                              \
+    cfg = cudaLaunchConfig_t{};                                                                 \
+    cfg.gridDim = dim3(grid, 1, 1);                                                             \
+    cfg.blockDim = dim3(kThreads, 1, 1);                                                        \
+    cfg.dynamicSmemBytes = smem;                                                                \
+    cfg.stream = stream;                                                                        \
+    attr[0].id = cudaLaunchAttributeClusterDimension;                                           \
+    attr[0].val.clusterDim.x = 2;                                                               \
+    attr[0].val.clusterDim.y = 1;                                                               \
+    attr[0].val.clusterDim.z = 1;                                                               \
+    cfg.attrs = attr;                                                                           \
+    cfg.numAttrs = 1;                                                                           \
+  }                                                                                             \
+  cudaError_t gemm_max_clusters_pair##BN(size_t smem, int* clusters) {                          \
+    cudaLaunchConfig_t cfg;                                                                     \
+    cudaLaunchAttribute attr[1];                                                                \
+    pair_config_##BN(cfg, attr, 2, smem, nullptr);                                              \
+    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2>, &cfg);               \
+  }                                                                                             \
+  cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,                  \
+                                   const CUtensorMap& c, const Params& p, int grid,             \
+                                   size_t smem, cudaStream_t stream) {                          \
+    cudaLaunchConfig_t cfg;                                                                     \
+    cudaLaunchAttribute attr[1];                                                                \
+    pair_config_##BN(cfg, attr, grid, smem, stream);                                            \
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2>, a, b, c, p);                         \
+  }                                                                                             \
   }

@@ -64,6 +64,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   return true;
 }
 
+// As wait_bounded, with cluster-scope acquire when other CTAs arrive on `bar`.
+template <int CG>
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     const Params& p, int detail) {
+  if constexpr (CG == 1) {
+    return wait_bounded(bar, parity, p, detail);
+  } else {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait_cluster(bar, parity)) {
+      if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+        record_error(p.status, kStatusTimeout, detail);
+        return false;
+      }
+    }
+    return true;
+  }
+}
+
 // Grouped tile order: tiles are taken `raster_group` tile rows at a time,
 // column by column inside a group.
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -92,13 +111,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int BN>
+// BN: output tile width.  CG: CTAs per tile (1, or 2 for a CTA pair that
+// computes a 256 x BN tile with cta_group::2 MMAs: each CTA loads its own 128
+// rows of A and BN/2 rows of B, the even CTA issues the MMAs for both, and
+// each CTA's TMEM receives its own 128 rows of the accumulator).
+template <int BN, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const Params p) {
-  constexpr uint32_t kStageB = BN * kBK * 2;
-  constexpr uint32_t kStage = kStageA + kStageB;
+  static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+  constexpr int kBRows = BN / CG;                    // B rows this CTA loads
+  constexpr uint32_t kStageB = kBRows * kBK * 2;
+  constexpr uint32_t kStage = kStageA + kStageB;     // bytes per slot, this CTA
   constexpr uint32_t kChunks = BN / kStoreCols;
+  constexpr int kTileM = kBM * CG;                   // output rows per tile
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B
@@ -123,6 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t tmem_cols = static_cast<uint32_t>(p.tmem_cols);
+  // Position in the CTA pair (always 0 without one).
+  const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = static_cast<int>(blockIdx.x) / CG;      // tile walker id
+  const int units = static_cast<int>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -131,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
-      ptx::mbar_init(tempty_bar(a), kEpiWarps);
+      // Every epilogue warp of every CTA of the tile releases the accumulator.
+      ptx::mbar_init(tempty_bar(a), kEpiWarps * CG);
     }
     ptx::mbar_init(done_bar, 1);
     ptx::fence_barrier_init();
@@ -142,11 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.tma_store) ptx::tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), tmem_cols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), tmem_cols);
+    ptx::tmem_relinquish<CG>();
   }
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2)
+    ptx::cluster_sync();  // peer barriers initialised before any remote arrive / TMA
+  else
+    __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
@@ -157,18 +192,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-slot: used at all / parity of last use
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < p.num_tiles; t += units) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
+        const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
+        const int b_row = nb * BN + static_cast<int>(rank) * kBRows;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(full_bar(stage), kStage);
           const uint32_t sa = sbase + stage * kStage;
-          ptx::tma_load_2d(sa, &tmA, kb * kBK, mb * kBM, full_bar(stage));
-          ptx::tma_load_2d(sa + kStageA, &tmB, kb * kBK, nb * BN, full_bar(stage));
+          if constexpr (CG == 2) {
+            // Both CTAs' copies count on the leader's full barrier; only the
+            // leader announces the bytes (of both CTAs).
+            const uint32_t fb = ptx::map_shared_rank(full_bar(stage), 0);
+            if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), kStage * CG);
+            ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
+            ptx::tma_load_2d_pair(sa + kStageA, &tmB, kb * kBK, b_row, fb);
+          } else {
+            ptx::mbar_arrive_expect_tx(full_bar(stage), kStage);
+            ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
+            ptx::tma_load_2d(sa + kStageA, &tmB, kb * kBK, b_row, full_bar(stage));
+          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -177,22 +223,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // Every copy this thread started must have landed before the CTA exits.
-      for (int s = 0; s < S; ++s)
-        if (issued & (1u << s))
-          wait_bounded(full_bar(s), (issued_parity >> s) & 1u, p, kDetailProducerDrain);
+      // Every copy this CTA pair started must have landed before it exits: the
+      // leader's full barriers count the bytes of both CTAs (the final
+      // cluster barrier keeps the peer resident until then).
+      if (leader) {
+        for (int s = 0; s < S; ++s)
+          if (issued & (1u << s))
+            wait_bounded(full_bar(s), (issued_parity >> s) & 1u, p, kDetailProducerDrain);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty)) break;
+      for (int t = unit; ok && t < p.num_tiles; t += units) {
+        if (!wait_bounded_cluster<CG>(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty))
+          break;
         ptx::tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -208,24 +259,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units).
-            ptx::mma_f16_ss(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
-                            (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+                                (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(empty_bar(stage));
+          if constexpr (CG == 2)
+            ptx::mma_commit_multicast_pair(empty_bar(stage), 0x3);
+          else
+            ptx::mma_commit<1>(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(tfull_bar(acc));
+        if constexpr (CG == 2)
+          ptx::mma_commit_multicast_pair(tfull_bar(acc), 0x3);
+        else
+          ptx::mma_commit<1>(tfull_bar(acc));
         if (++acc == p.num_acc) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // All MMAs this thread issued must be complete before TMEM is freed.
-      ptx::mma_commit(done_bar);
+      ptx::mma_commit<CG>(done_bar);
       wait_bounded(done_bar, 0, p, kDetailMmaDrain);
     }
     __syncwarp();
@@ -238,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     int buf = 0;
     const bool bf16 = p.bf16 != 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int t = unit; t < p.num_tiles; t += units) {
       int mb, nb;
       tile_coords(t, p, mb, nb);
       int ready = 1;
@@ -247,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ready) break;
       ptx::tc_fence_after_sync();
 
-      const int row0 = mb * kBM + q * 32;
+      const int row0 = mb * kTileM + static_cast<int>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       if (row0 < p.M) {
@@ -285,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             uint8_t* sb = my_stage + buf * kStoreBuf;
             // Row `lane` is 128 B; 16-byte chunk j lands at j ^ (row % 8),
-            // the layout of a 128-byte-swizzled TMA box (bank-conflict free).
+            // the layout of a 128-byte-swizzled TMA box.
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
@@ -316,7 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // This warp's TMEM reads of accumulator `acc` are complete (wait::ld).
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          ptx::mbar_arrive_cluster(ptx::map_shared_rank(tempty_bar(acc), 0));
+        else
+          ptx::mbar_arrive(tempty_bar(acc));
+      }
       if (++acc == p.num_acc) {
         acc = 0;
         acc_phase ^= 1u;
@@ -327,10 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CG == 2)
+    ptx::cluster_sync();  // neither CTA leaves while its peer may still touch its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, tmem_cols);
+    ptx::tmem_dealloc<CG>(tmem_base, tmem_cols);
   }
 }
 

@@ -50,9 +50,11 @@ struct Params {
   unsigned long long timeout_ns;
 };
 
-// Shared memory a CTA needs for a given tile width / ring depth / staging.
-inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs) {
-  const size_t stage = static_cast<size_t>(kStageA) + static_cast<size_t>(bn) * kBK * 2;
+// Shared memory a CTA needs for a given tile width / ring depth / staging;
+// with a CTA pair (cta_group 2) each CTA holds half of the tile's B rows.
+inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs, int cta_group = 1) {
+  const size_t stage =
+      static_cast<size_t>(kStageA) + static_cast<size_t>(bn / cta_group) * kBK * 2;
   return kAlignSlack + stage * static_cast<size_t>(stages) +
          static_cast<size_t>(kEpiWarps) * store_bufs * kStoreBuf + kBarrierBytes;
 }

@@ -21,6 +21,17 @@ SPGEMM_DECLARE_BN(128)
 SPGEMM_DECLARE_BN(256)
 #undef SPGEMM_DECLARE_BN
 
+// CTA-pair instances (cluster of 2, cta_group::2 MMAs, 256 x BN tiles).
+#define SPGEMM_DECLARE_PAIR(BN)                                                            \
+  cudaError_t gemm_set_smem_pair##BN(size_t smem);                                         \
+  cudaError_t gemm_max_clusters_pair##BN(size_t smem, int* clusters);                      \
+  cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,             \
+                                   const CUtensorMap& c, const Params& p, int grid,        \
+                                   size_t smem, cudaStream_t stream);
+SPGEMM_DECLARE_PAIR(128)
+SPGEMM_DECLARE_PAIR(256)
+#undef SPGEMM_DECLARE_PAIR
+
 // Copy the rows of A (M x K) and/or B (N x K) into zero-padded scratch with
 // row pitch Kp (a multiple of 8 elements, so every row is 16-byte aligned).
 cudaError_t launch_pad_operands(const uint16_t* A, int64_t M, uint16_t* Ap, const uint16_t* B,

@@ -58,15 +58,48 @@ def test_every_ring_depth_bit_exact_with_persistent_tiles(stages):
     # 9 K slices so the ring wraps; 16 tiles over 2 CTAs so each CTA walks 8
     # tiles and both accumulators change hands several times.
     A, B = _int_inputs(512, 1024, 576, "f16", seed=100 + stages)
-    C, info, canary = gu.run_device(A, B, "f16", stages=stages, max_ctas=2)
+    C, info, canary = gu.run_device(A, B, "f16", stages=stages, max_ctas=2, cta_group=1)
     assert canary and info["grid"] == 2 and info["stages"] == stages
+    _assert_bit_exact(A, B, "f16", C)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_cta_pair_every_ring_depth_bit_exact(stages):
+    # CTA pairs (256-row tiles): 8 K slices, 12 pair tiles over 2 clusters.
+    tile_n = 256 if stages <= 6 else 128
+    A, B = _int_inputs(768, 1024, 512, "f16", seed=200 + stages)
+    C, info, canary = gu.run_device(A, B, "f16", stages=stages, cta_group=2, tile_n=tile_n,
+                                    max_ctas=4)
+    assert canary and info["cta_group"] == 2 and info["grid"] == 4
+    _assert_bit_exact(A, B, "f16", C)
+
+
+@pytest.mark.parametrize("shape", [(1, 8, 8), (129, 130, 72), (255, 257, 136), (256, 256, 64),
+                                   (257, 384, 264), (513, 1000, 1000), (300, 200, 8)])
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_cta_pair_edge_shapes(shape, tile_n):
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, seed=M + 3 * N + 5 * K + tile_n)
+    C, info, canary = gu.run_device(A, B, "f16", cta_group=2, tile_n=tile_n)
+    st, _, _ = gu.check_full(A, B, "f16", C)
+    assert canary and st["ok"] and info["cta_group"] == 2, (shape, st, info)
+
+
+def test_cta_pair_bf16_gelu_and_single_buffer():
+    A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=512, N=768, K=512)
+    C, info, canary = gu.run_device(A, B, "bf16", epilogue="gelu", cta_group=2, stages=5)
+    st, _, _ = gu.check_full(A, B, "bf16", C, epilogue="gelu")
+    assert canary and st["ok"] and info["cta_group"] == 2, st
+    A, B = _int_inputs(512, 512, 384, "f16", seed=33)
+    C, info, canary = gu.run_device(A, B, "f16", cta_group=2, stages=1, variant="single_buffer")
+    assert canary and info["cta_group"] == 2 and info["accumulators"] == 1
     _assert_bit_exact(A, B, "f16", C)
 
 
 @pytest.mark.parametrize("tile_n", [64, 128, 256])
 def test_each_tile_width_bit_exact(tile_n):
     A, B = _int_inputs(384, 640, 320, "f16", seed=7)
-    C, info, canary = gu.run_device(A, B, "f16", tile_n=tile_n, max_ctas=3)
+    C, info, canary = gu.run_device(A, B, "f16", tile_n=tile_n, max_ctas=3, cta_group=1)
     assert canary and info["tile_n"] == tile_n
     _assert_bit_exact(A, B, "f16", C)
 
@@ -80,7 +113,8 @@ def test_bf16_integer_bit_exact():
 
 def test_single_buffer_variant_bit_exact():
     A, B = _int_inputs(384, 512, 640, "f16", seed=11)
-    C, info, canary = gu.run_device(A, B, "f16", stages=1, variant="single_buffer", max_ctas=4)
+    C, info, canary = gu.run_device(A, B, "f16", stages=1, variant="single_buffer", max_ctas=4,
+                                    cta_group=1)
     assert canary and info["accumulators"] == 1 and info["stages"] == 1
     _assert_bit_exact(A, B, "f16", C)
 
@@ -193,10 +227,16 @@ def test_plan_mismatch_and_aliasing_rejected():
 def test_smem_budget_reported_not_clamped():
     import software_pipelined_tiled_gemm_gb300 as sg
     with pytest.raises(sg.GemmError) as ei:
-        sg.Plan(4096, 4096, 4096, "f16", stages=5, tile_n=256)
+        sg.Plan(4096, 4096, 4096, "f16", stages=5, tile_n=256, cta_group=1)
     assert ei.value.status == sg.GEMM_ERR_SMEM_BUDGET
-    p = sg.Plan(4096, 4096, 4096, "f16", stages=6)      # auto: narrower tile fits
-    assert p.info()["stages"] == 6 and p.info()["tile_n"] < 256
+    with pytest.raises(sg.GemmError) as ei:
+        sg.Plan(4096, 4096, 4096, "f16", stages=7, tile_n=256, cta_group=2)
+    assert ei.value.status == sg.GEMM_ERR_SMEM_BUDGET
+    p = sg.Plan(4096, 4096, 4096, "f16", stages=6)      # auto: 256x256 CTA pairs fit 6 slots
+    assert p.info()["stages"] == 6 and p.info()["cta_group"] == 2 and p.info()["tile_n"] == 256
+    p.close()
+    p = sg.Plan(4096, 4096, 4096, "f16", stages=6, cta_group=1)   # single CTA: narrower tile
+    assert p.info()["tile_n"] < 256
     p.close()
 
 
@@ -245,6 +285,10 @@ def _full_size(name, stages=4, variant="pipelined", count=3000, **tuning):
 @pytest.mark.parametrize("stages", [2, 3, 4, 5, 6])
 def test_config_4096_stage_sweep(stages):
     _full_size("gemm_4096_f16", stages=stages)
+
+
+def test_config_4096_single_cta_tiles():
+    _full_size("gemm_4096_f16", stages=4, cta_group=1)
 
 
 def test_config_8192_pipelined():
