@@ -246,6 +246,8 @@ def main():
             dist.barrier()
 
     epi = None if w.epilogue == "none" else "gelu"
+    if args.variant == "single_buffer":
+        args.stages = 1
     A_cpu, B_cpu = gemm_inputs.make(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
