@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--tail-split", type=int, default=0,
+                    help="K-splitting of the last partial wave: 0 auto, -1 off, k >= 2 forced")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -252,7 +254,8 @@ def main():
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
     plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
-                   tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group)
+                   tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group,
+                   tail_split=args.tail_split)
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
     a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
@@ -305,7 +308,7 @@ def main():
         hC = torch.empty(w.M, w.N, dtype=A_cpu.dtype).pin_memory()
         eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
                         tile_n=args.tile_n, raster_group=args.raster_group,
-                        cta_group=args.cta_group)
+                        cta_group=args.cta_group, tail_split=args.tail_split)
         eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
         barrier()
         t0 = time.perf_counter()
@@ -360,7 +363,8 @@ def main():
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],
-                "cta_group": info["cta_group"],
+                "cta_group": info["cta_group"], "tail_splits": info["tail_splits"],
+                "tail_tiles": info["tail_tiles"],
                 "l2": ("inputs larger than L2 (%d MiB of operands vs %d MiB L2); no flush"
                        % ((w.M * w.K + w.N * w.K) * 2 >> 20, L2_BYTES >> 20))
                 if (w.M * w.K + w.N * w.K) * 2 > L2_BYTES else "operands fit in L2 (warm)",

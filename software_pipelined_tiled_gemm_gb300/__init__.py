@@ -56,7 +56,7 @@ GEMM_SINGLE_BUFFER = 1
 class GemmTuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
-                ("timeout_ns", ctypes.c_int64)]
+                ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -66,7 +66,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("num_tiles", ctypes.c_int64), ("smem_bytes", ctypes.c_size_t),
                 ("pads_operands", ctypes.c_int), ("tma_store", ctypes.c_int),
                 ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int),
-                ("cta_group", ctypes.c_int)]
+                ("cta_group", ctypes.c_int), ("tail_tiles", ctypes.c_int64),
+                ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -231,7 +232,8 @@ class Plan:
     """Owns one gemm_plan_t."""
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
-                 tile_n=0, raster_group=0, max_ctas=0, cta_group=0, timeout_ns=0):
+                 tile_n=0, raster_group=0, max_ctas=0, cta_group=0, tail_split=0,
+                 timeout_ns=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -240,7 +242,7 @@ class Plan:
         self.device = int(device)
         self._h = None
         tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
-                            int(timeout_ns))
+                            int(tail_split), int(timeout_ns))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")

@@ -111,6 +111,9 @@ struct gemm_plan {
   unsigned long long timeout_ns = kDefaultTimeoutNs;
 
   int* d_status = nullptr;       // [0] code, [1] detail
+  int64_t dp_tiles = 0;          // tiles run whole
+  int tail_splits = 1;           // narrow tiles per tail tile (cut along N)
+  int64_t num_units = 0;
   uint16_t* scratch = nullptr;   // padded copies of A and/or B
   size_t scratch_bytes = 0;
 
@@ -119,7 +122,7 @@ struct gemm_plan {
   const void* mapB_ptr = nullptr;
   const void* mapC_ptr = nullptr;
   int64_t mapK = -1;
-  CUtensorMap tmA{}, tmB{}, tmC{};
+  CUtensorMap tmA{}, tmB{}, tmBt{}, tmC{};   // tmBt: B box of a narrow tail tile
 
   // device staging for gemm_run_host
   void* hA = nullptr;
@@ -181,14 +184,15 @@ cudaError_t set_smem(int bn, int cg, size_t smem) {
 }
 
 cudaError_t launch(int bn, int cg, const CUtensorMap& a, const CUtensorMap& b,
-                   const CUtensorMap& c, const Params& p, int grid, size_t smem, cudaStream_t s) {
+                   const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid,
+                   size_t smem, cudaStream_t s) {
   if (cg == 2)
-    return bn == 128 ? gemm_launch_pair128(a, b, c, p, grid, smem, s)
-                     : gemm_launch_pair256(a, b, c, p, grid, smem, s);
+    return bn == 128 ? gemm_launch_pair128(a, b, bt, c, p, grid, smem, s)
+                     : gemm_launch_pair256(a, b, bt, c, p, grid, smem, s);
   switch (bn) {
-    case 64: return gemm_launch_bn64(a, b, c, p, grid, smem, s);
-    case 128: return gemm_launch_bn128(a, b, c, p, grid, smem, s);
-    default: return gemm_launch_bn256(a, b, c, p, grid, smem, s);
+    case 64: return gemm_launch_bn64(a, b, bt, c, p, grid, smem, s);
+    case 128: return gemm_launch_bn128(a, b, bt, c, p, grid, smem, s);
+    default: return gemm_launch_bn256(a, b, bt, c, p, grid, smem, s);
   }
 }
 
@@ -235,13 +239,16 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     return fail(GEMM_ERR_INVALID_ARG, "the single-buffer variant has exactly 1 stage (got %d)",
                 stages);
   if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
-  int want_bn = 0, want_group = 0, want_ctas = 0, want_cg = 0;
+  int want_bn = 0, want_group = 0, want_ctas = 0, want_cg = 0, want_split = 0;
   unsigned long long timeout = kDefaultTimeoutNs;
   if (tuning) {
     want_bn = tuning->tile_n;
     want_group = tuning->raster_group;
     want_ctas = tuning->max_ctas;
     want_cg = tuning->cta_group;
+    want_split = tuning->tail_split;
+    if (want_split < -1 || want_split == 1 || want_split > kMaxTailSplits)
+      return fail(GEMM_ERR_INVALID_ARG, "tail_split %d not in {-1, 0, 2, 3, 4}", want_split);
     if (want_bn != 0 && want_bn != 64 && want_bn != 128 && want_bn != 256)
       return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", want_bn);
     if (want_cg < 0 || want_cg > 2)
@@ -347,15 +354,47 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->raster_group = want_group > 0 ? want_group : (chosen_cg == 2 ? 8 : 16);
   if (p->tiles_m > 0)
     p->raster_group = static_cast<int>(std::min<int64_t>(p->raster_group, p->tiles_m));
+  // Walkers: persistent CTAs (or CTA pairs) that can be resident at once.
+  int walkers;
   if (chosen_cg == 2) {
-    int clusters = chosen_clusters;
-    if (want_ctas > 0) clusters = std::min(clusters, std::max(1, want_ctas / 2));
-    p->grid = 2 * static_cast<int>(std::min<int64_t>(p->num_tiles, clusters));
+    walkers = chosen_clusters;
+    if (want_ctas > 0) walkers = std::min(walkers, std::max(1, want_ctas / 2));
   } else {
-    int cap = p->sm_count;
-    if (want_ctas > 0) cap = std::min(cap, want_ctas);
-    p->grid = static_cast<int>(std::min<int64_t>(p->num_tiles, cap));
+    walkers = p->sm_count;
+    if (want_ctas > 0) walkers = std::min(walkers, want_ctas);
   }
+  // Cut the tiles of the last, partial wave along N into narrower tiles
+  // (at least 64 columns each) so that wave keeps more walkers busy for a
+  // shorter time.  No reduction is needed: the narrow tiles are disjoint.
+  // Narrow MMAs re-read A from shared memory for fewer columns, so the
+  // automatic choice only cuts a last wave that is at most a quarter full
+  // (measured on GB300: a 4-way cut of 8 leftover 256x256 tiles gains ~3 %,
+  // 2-way cuts of waves a third to half full lose 2 %).
+  p->dp_tiles = p->num_tiles;
+  p->tail_splits = 1;
+  if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
+    const int64_t rem = p->num_tiles % walkers;
+    const int max_s = std::min(kMaxTailSplits, p->bn / kStoreCols);
+    if (rem > 0 && (want_split >= 2 || rem * 4 <= walkers)) {
+      int64_t S = want_split >= 2 ? want_split : std::min<int64_t>(walkers / rem, max_s);
+      if (S >= 2 && S <= max_s && p->bn % S == 0) {
+        p->dp_tiles = p->num_tiles - rem;
+        p->tail_splits = static_cast<int>(S);
+      } else if (want_split >= 2) {
+        delete p;
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "tail_split %d does not divide tile width %d into >= %d-column tiles",
+                    want_split, p->bn, kStoreCols);
+      }
+    }
+  }
+  const int64_t tail = p->num_tiles - p->dp_tiles;
+  p->num_units = p->dp_tiles + tail * p->tail_splits;
+  if (p->num_units > kMaxDim) {
+    delete p;
+    return fail(GEMM_ERR_INVALID_ARG, "too many work units");
+  }
+  p->grid = chosen_cg * static_cast<int>(std::min<int64_t>(p->num_units, walkers));
 
   // The limit is per kernel function, shared by every plan on the device:
   // always raise it to the device maximum, never to this plan's own size, so
@@ -472,6 +511,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
                    static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (st != GEMM_OK) return st;
+    if (plan->tail_splits > 1) {
+      st = encode_2d(&plan->tmBt, plan->dtype, effB, Keff, N, Keff, kBK,
+                     static_cast<uint32_t>(plan->bn / plan->tail_splits / plan->cg),
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+      if (st != GEMM_OK) return st;
+    } else {
+      plan->tmBt = plan->tmB;
+    }
     plan->mapB_ptr = effB;
   }
   plan->mapK = Keff;
@@ -507,9 +554,17 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.ldc = N;
   prm.status = plan->d_status;
   prm.timeout_ns = plan->timeout_ns;
+  prm.dp_tiles = static_cast<int>(plan->dp_tiles);
+  prm.tail_splits = plan->tail_splits;
+  prm.num_units = static_cast<int>(plan->num_units);
+  prm.idesc_tail = ptx::instr_desc_f16(kBM * plan->cg, plan->bn / plan->tail_splits,
+                                       plan->dtype == GEMM_BF16);
+  // One row of tiles across the whole grid: every CTA reads the same A rows,
+  // so stagger where each starts along K.
+  prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
 
-  cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmC, prm, plan->grid,
-                         plan->smem, stream);
+  cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC, prm,
+                         plan->grid, plan->smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
   ++kernels;
   plan->last_pads = (padA || padB) ? 1 : 0;
@@ -587,6 +642,9 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->kernels_per_run = plan->last_kernels;
   info->sm_count = plan->sm_count;
   info->cta_group = plan->cg;
+  info->tail_tiles = plan->num_tiles - plan->dp_tiles;
+  info->tail_splits = plan->tail_splits;
+  info->work_units = plan->num_units;
   return GEMM_OK;
 }
 

@@ -1,4 +1,5 @@
-// gemm_instance.cuh -- defines the launcher pair of one kernel instance.
+// gemm_instance.cuh -- defines the launchers of one kernel shape (both the
+// plain instance and the one that can run narrow tail tiles).
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -7,13 +8,21 @@
 #define SPGEMM_DEFINE_BN(BN)                                                                   \
   namespace spgemm {                                                                           \
   cudaError_t gemm_set_smem_bn##BN(size_t smem) {                                              \
-    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<BN, 1, false>,                         \
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,          \
+                                         static_cast<int>(smem));                              \
+    if (e != cudaSuccess) return e;                                                            \
+    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 1, true>,                                   \
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,                   \
                                 static_cast<int>(smem));                                       \
   }                                                                                            \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,                   \
-                                 const CUtensorMap& c, const Params& p, int grid, size_t smem, \
+                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid, size_t smem, \
                                  cudaStream_t stream) {                                        \
-    gemm_tn_kernel<BN, 1><<<grid, kThreads, smem, stream>>>(a, b, c, p);                          \
+    if (p.tail_splits > 1)                                                                     \
+      gemm_tn_kernel<BN, 1, true><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);               \
+    else                                                                                       \
+      gemm_tn_kernel<BN, 1, false><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);              \
     return cudaGetLastError();                                                                 \
   }                                                                                            \
   }
@@ -21,7 +30,11 @@
 #define SPGEMM_DEFINE_PAIR(BN)                                                                  \
   namespace spgemm {                                                                            \
   cudaError_t gemm_set_smem_pair##BN(size_t smem) {                                             \
-    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 2>,                                          \
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<BN, 2, false>,                          \
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,           \
+                                         static_cast<int>(smem));                               \
+    if (e != cudaSuccess) return e;                                                             \
+    return cudaFuncSetAttribute(gemm_tn_kernel<BN, 2, true>,                                    \
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,                    \
                                 static_cast<int>(smem));                                        \
   }                                                                                             \
@@ -43,14 +56,16 @@
     cudaLaunchConfig_t cfg;                                                                     \
     cudaLaunchAttribute attr[1];                                                                \
     pair_config_##BN(cfg, attr, 2, smem, nullptr);                                              \
-    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2>, &cfg);               \
+    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false>, &cfg);        \
   }                                                                                             \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,                  \
-                                   const CUtensorMap& c, const Params& p, int grid,             \
+                                   const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid,             \
                                    size_t smem, cudaStream_t stream) {                          \
     cudaLaunchConfig_t cfg;                                                                     \
     cudaLaunchAttribute attr[1];                                                                \
     pair_config_##BN(cfg, attr, grid, smem, stream);                                            \
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2>, a, b, c, p);                         \
+    if (p.tail_splits > 1)                                                                      \
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, true>, a, b, bt, c, p);                 \
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, false>, a, b, bt, c, p);                  \
   }                                                                                             \
   }

@@ -95,6 +95,26 @@ __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int
   nb = r / rows;
 }
 
+// Work unit -> (tile, sub-tile).  A tail tile is cut along N into
+// tail_splits narrow tiles; every other tile is one unit.
+__device__ __forceinline__ void unit_info(int u, const Params& p, int& tile, int& sub) {
+  if (u < p.dp_tiles) {
+    tile = u;
+    sub = -1;
+  } else {
+    const int v = u - p.dp_tiles;
+    tile = p.dp_tiles + v / p.tail_splits;
+    sub = v - (v / p.tail_splits) * p.tail_splits;
+  }
+}
+
+// First K slice of a unit's loop: 0, or spread over the K range by unit index.
+__device__ __forceinline__ int k_start(int u, int units, const Params& p) {
+  if (!p.k_rotate) return 0;
+  const int n = units < p.num_units ? units : p.num_units;
+  return static_cast<int>((static_cast<int64_t>(u % n) * p.k_blocks) / n);
+}
+
 __device__ __forceinline__ float gelu_tanh(float x) {
   // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)); this form cannot produce
   // inf/inf for large |u| (x -> x for u -> +inf, x -> -0 for u -> -inf).
@@ -115,15 +135,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 // computes a 256 x BN tile with cta_group::2 MMAs: each CTA loads its own 128
 // rows of A and BN/2 rows of B, the even CTA issues the MMAs for both, and
 // each CTA's TMEM receives its own 128 rows of the accumulator).
-template <int BN, int CG>
+// kSplit: this instance can run narrow tail tiles (BN / tail_splits wide,
+// B loaded through tmBt); the instance used by plans without a tail split
+// has that code compiled out.
+template <int BN, int CG, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const Params p) {
+                   const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
+                   const Params p) {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
   constexpr int kBRows = BN / CG;                    // B rows this CTA loads
   constexpr uint32_t kStageB = kBRows * kBK * 2;
   constexpr uint32_t kStage = kStageA + kStageB;     // bytes per slot, this CTA
-  constexpr uint32_t kChunks = BN / kStoreCols;
   constexpr int kTileM = kBM * CG;                   // output rows per tile
 
   extern __shared__ uint8_t smem_raw[];
@@ -171,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&tmA);
     ptx::tma_prefetch_desc(&tmB);
+    if (kSplit) ptx::tma_prefetch_desc(&tmBt);
     if (p.tma_store) ptx::tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
@@ -192,12 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-slot: used at all / parity of last use
       bool ok = true;
-      for (int t = unit; ok && t < p.num_tiles; t += units) {
-        int mb, nb;
+      for (int u = unit; ok && u < p.num_units; u += units) {
+        int t, sub, mb, nb;
+        unit_info(u, p, t, sub);
         tile_coords(t, p, mb, nb);
+        const bool narrow = kSplit && sub >= 0;
+        const int n_width = narrow ? BN / p.tail_splits : BN;   // columns of this unit
+        const int b_rows = n_width / CG;                        // B rows this CTA loads
         const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
-        const int b_row = nb * BN + static_cast<int>(rank) * kBRows;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const int b_row = nb * BN + (narrow ? sub * n_width : 0) + static_cast<int>(rank) * b_rows;
+        const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
+        const uint32_t bytes = (kStageA + static_cast<uint32_t>(b_rows) * kBK * 2u) * CG;
+        const int k0 = k_start(u, units, p);
+        for (int i = 0, kb = k0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
             ok = false;
             break;
@@ -207,13 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Both CTAs' copies count on the leader's full barrier; only the
             // leader announces the bytes (of both CTAs).
             const uint32_t fb = ptx::map_shared_rank(full_bar(stage), 0);
-            if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), kStage * CG);
+            if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-            ptx::tma_load_2d_pair(sa + kStageA, &tmB, kb * kBK, b_row, fb);
+            ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
           } else {
-            ptx::mbar_arrive_expect_tx(full_bar(stage), kStage);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-            ptx::tma_load_2d(sa + kStageA, &tmB, kb * kBK, b_row, full_bar(stage));
+            ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -241,12 +272,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = unit; ok && t < p.num_tiles; t += units) {
+      for (int u = unit; ok && u < p.num_units; u += units) {
+        int t, sub;
+        unit_info(u, p, t, sub);
+        const uint32_t idesc = (kSplit && sub >= 0) ? p.idesc_tail : p.idesc;
         if (!wait_bounded_cluster<CG>(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty))
           break;
         ptx::tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks; ++kb) {  // iteration count (slices may be rotated)
           if (!wait_bounded(full_bar(stage), phase, p, kDetailMmaFull)) {
             ok = false;
             break;
@@ -259,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units).
-            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc,
+            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                 (kb | k) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)
@@ -295,9 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     int buf = 0;
     const bool bf16 = p.bf16 != 0;
-    for (int t = unit; t < p.num_tiles; t += units) {
-      int mb, nb;
+    for (int u = unit; u < p.num_units; u += units) {
+      int t, sub, mb, nb;
+      unit_info(u, p, t, sub);
       tile_coords(t, p, mb, nb);
+      const bool narrow = kSplit && sub >= 0;
+      const int n_width = narrow ? BN / p.tail_splits : BN;
+      const int n0 = nb * BN + (narrow ? sub * n_width : 0);
+      const uint32_t chunks = static_cast<uint32_t>(n_width) / kStoreCols;
       int ready = 1;
       if (lane == 0) ready = wait_bounded(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
       ready = __shfl_sync(0xffffffffu, ready, 0);
@@ -309,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                              static_cast<uint32_t>(acc * BN);
       if (row0 < p.M) {
 #pragma unroll 1
-        for (uint32_t c = 0; c < kChunks; ++c) {
-          const int col0 = nb * BN + static_cast<int>(c) * kStoreCols;
+        for (uint32_t c = 0; c < chunks; ++c) {
+          const int col0 = n0 + static_cast<int>(c) * kStoreCols;
           if (col0 >= p.N) break;
           uint32_t r0[32], r1[32];
           ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols, r0);
@@ -357,14 +396,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             buf = (buf + 1 == p.store_bufs) ? 0 : buf + 1;
           } else {
-            const int row = row0 + lane;
-            if (row < p.M) {
-              uint16_t* crow = reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row) * p.ldc;
-              const int ncols = min(kStoreCols, p.N - col0);
+            // C's pitch or address is not 16-byte aligned, so no TMA store:
+            // stage the 32 x 64 chunk in shared memory (same swizzled layout)
+            // and write it out a row at a time, each store instruction
+            // covering 64 contiguous bytes of one row.
+            __syncwarp();  // the previous chunk's reads of the buffer are done
+            uint8_t* sb = my_stage;
 #pragma unroll
-              for (int j = 0; j < kStoreCols; ++j) {
-                if (j < ncols)
-                  crow[col0 + j] = static_cast<uint16_t>(pk[j >> 1] >> ((j & 1) * 16));
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+              *reinterpret_cast<uint4*>(sb + off) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            __syncwarp();
+            const int ncols = min(kStoreCols, p.N - col0);
+            const int nrows = min(32, p.M - row0);
+#pragma unroll 1
+            for (int r = 0; r < nrows; ++r) {
+              uint16_t* crow =
+                  reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row0 + r) * p.ldc + col0;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int cc = lane + 32 * h;
+                if (cc < ncols) {
+                  const uint32_t off = static_cast<uint32_t>(r) * 128u +
+                                       ((static_cast<uint32_t>(cc >> 3) ^ (static_cast<uint32_t>(r) & 7u)) << 4) +
+                                       static_cast<uint32_t>(cc & 7) * 2u;
+                  crow[cc] = *reinterpret_cast<const uint16_t*>(sb + off);
+                }
               }
             }
           }

@@ -21,6 +21,8 @@ constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
 
+constexpr int kMaxTailSplits = 4;    // narrow tiles a tail tile may be cut into (N >= 64 each)
+
 // Where a device-side wait ran out (status word [1]): role << 16 | wait id.
 constexpr int kDetailProducerEmpty = (1 << 16) | 1;
 constexpr int kDetailProducerDrain = (1 << 16) | 2;
@@ -48,6 +50,19 @@ struct Params {
   int64_t ldc;
   int* status;           // device status word: [0] code, [1] detail
   unsigned long long timeout_ns;
+  // Work units: tiles [0, dp_tiles) run whole; each remaining ("tail") tile
+  // is cut along N into tail_splits narrower tiles of BN / tail_splits
+  // columns, so the last, partial wave keeps more CTAs busy for a shorter
+  // time.  num_units = dp_tiles + tail tiles * tail_splits.  Narrow tiles use
+  // the B tensor map with the smaller box and the MMA descriptor idesc_tail.
+  int dp_tiles;
+  int tail_splits;
+  int num_units;
+  uint32_t idesc_tail;
+  // 1: each unit starts its K loop at a different slice (wrapping around),
+  // so CTAs that share the same A rows do not all read the same A slice at
+  // the same time (used when a single row of tiles spans the whole grid).
+  int k_rotate;
 };
 
 // Shared memory a CTA needs for a given tile width / ring depth / staging;

@@ -14,7 +14,8 @@ namespace spgemm {
 #define SPGEMM_DECLARE_BN(BN)                                                              \
   cudaError_t gemm_set_smem_bn##BN(size_t smem);                                           \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,               \
-                                 const CUtensorMap& c, const Params& p, int grid, size_t smem, \
+                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, \
+                                 int grid, size_t smem,                                    \
                                  cudaStream_t stream);
 SPGEMM_DECLARE_BN(64)
 SPGEMM_DECLARE_BN(128)
@@ -26,7 +27,8 @@ SPGEMM_DECLARE_BN(256)
   cudaError_t gemm_set_smem_pair##BN(size_t smem);                                         \
   cudaError_t gemm_max_clusters_pair##BN(size_t smem, int* clusters);                      \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,             \
-                                   const CUtensorMap& c, const Params& p, int grid,        \
+                                   const CUtensorMap& bt, const CUtensorMap& c,            \
+                                   const Params& p, int grid,                              \
                                    size_t smem, cudaStream_t stream);
 SPGEMM_DECLARE_PAIR(128)
 SPGEMM_DECLARE_PAIR(256)

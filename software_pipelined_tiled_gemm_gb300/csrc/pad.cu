@@ -2,9 +2,13 @@
 // TMA engine (row pitch or base address not 16-byte aligned).
 //
 // dst[r, c] = src[r, c] for c < K and 0 for K <= c < Kp, Kp a multiple of 8.
-// Memory-bound: each thread emits one 16-byte store of 8 elements; source
-// elements are read with 2-byte loads because source rows may start at any
-// even address.  Both operands are handled by one launch.
+// Memory-bound.  Each thread emits one 16-byte store of 8 elements.  Its 8
+// source elements start at an arbitrary even byte address; they are taken
+// from the two 16-byte-aligned words that cover them (two vector loads,
+// shared with the neighbouring threads through L1) and shifted into place.
+// Where an aligned word would reach outside the source array (its first or
+// last few elements), the elements are read one by one instead.  Both
+// operands are handled by one launch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -12,6 +16,21 @@
 #include "launch.h"
 
 namespace spgemm {
+
+// Bytes [off, off + 16) of the 32-byte little-endian value (lo, hi), off even.
+__device__ __forceinline__ uint4 shift_window(const uint4& lo, const uint4& hi, uint32_t off) {
+  const uint32_t q = off >> 2;          // whole 32-bit words to skip (0..3)
+  const uint32_t sh = (off & 3u) * 8u;  // then 0 or 16 more bits
+  uint32_t a0, a1, a2, a3, a4;
+  switch (q) {
+    case 0: a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x; break;
+    case 1: a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y; break;
+    case 2: a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z; break;
+    default: a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w; break;
+  }
+  return make_uint4(__funnelshift_r(a0, a1, sh), __funnelshift_r(a1, a2, sh),
+                    __funnelshift_r(a2, a3, sh), __funnelshift_r(a3, a4, sh));
+}
 
 __global__ void __launch_bounds__(256) pad_operands_kernel(const uint16_t* __restrict__ A, int64_t M,
                                                            uint16_t* __restrict__ Ap,
@@ -28,17 +47,37 @@ __global__ void __launch_bounds__(256) pad_operands_kernel(const uint16_t* __res
     const int64_t w = isA ? v : v - nA;
     const int64_t r = w / vpr;
     const int64_t c0 = (w - r * vpr) * 8;
-    const uint16_t* s = (isA ? A : B) + r * K;
+    const uint16_t* src = isA ? A : B;
+    const int64_t rows = isA ? M : N;
     uint16_t* d = (isA ? Ap : Bp) + r * Kp + c0;
-    uint32_t word[4];
+    const int64_t valid = K - c0 < 8 ? (K - c0 > 0 ? K - c0 : 0) : 8;  // in-row elements
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (valid > 0) {
+      const uint16_t* s = src + r * K + c0;
+      const uintptr_t addr = reinterpret_cast<uintptr_t>(s);
+      const uintptr_t base = addr & ~static_cast<uintptr_t>(15);
+      const uintptr_t first = reinterpret_cast<uintptr_t>(src);
+      const uintptr_t end = reinterpret_cast<uintptr_t>(src + rows * K);  // one past the last element
+      if (base >= first && base + 32 <= end) {  // both aligned words inside the array
+        const uint4 lo = __ldg(reinterpret_cast<const uint4*>(base));
+        const uint4 hi = __ldg(reinterpret_cast<const uint4*>(base + 16));
+        out = shift_window(lo, hi, static_cast<uint32_t>(addr - base));
+      } else {
+        uint32_t wd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t c = c0 + 2 * j;
-      const uint32_t lo = c < K ? __ldg(s + c) : 0u;
-      const uint32_t hi = c + 1 < K ? __ldg(s + c + 1) : 0u;
-      word[j] = lo | (hi << 16);
+        for (int j = 0; j < 8; ++j)
+          if (j < valid) wd[j >> 1] |= static_cast<uint32_t>(__ldg(s + j)) << ((j & 1) * 16);
+        out = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+      if (valid < 8) {  // zero the elements past the end of the row
+        uint32_t wd[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j >= valid) wd[j >> 1] &= (j & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+        out = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
     }
-    *reinterpret_cast<uint4*>(d) = make_uint4(word[0], word[1], word[2], word[3]);
+    *reinterpret_cast<uint4*>(d) = out;
   }
 }
 
@@ -49,7 +88,7 @@ cudaError_t launch_pad_operands(const uint16_t* A, int64_t M, uint16_t* Ap, cons
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 16;
   if (blocks > cap) blocks = cap;
   pad_operands_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(A, M, Ap, B, N, Bp, K, Kp);
   return cudaGetLastError();

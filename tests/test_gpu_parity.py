@@ -348,3 +348,81 @@ def test_plans_with_different_rings_coexist():
         _assert_bit_exact(A, B, "f16", c.cpu())
     big.close()
     small.close()
+
+
+# ------------------------------------- narrow tail tiles (last wave) --
+
+@pytest.mark.parametrize("cta_group,splits", [(2, 2), (2, 4), (1, 2), (1, 4)])
+def test_tail_split_bit_exact_and_reusable(cta_group, splits):
+    # 12 tiles over 5 walkers: 10 whole tiles, the last 2 cut along N into
+    # `splits` narrow tiles.  The same plan runs three times.
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M = 768 if cta_group == 2 else 384
+    A, B = _int_inputs(M, 1024, 1024, "f16", seed=300 + splits)
+    plan = sg.Plan(M, 1024, 1024, "f16", stages=4, cta_group=cta_group, tile_n=256,
+                   max_ctas=5 * cta_group, tail_split=splits)
+    info = plan.info()
+    assert info["tail_tiles"] == 2 and info["tail_splits"] == splits
+    assert info["work_units"] == 10 + 2 * splits
+    a, b = A.cuda(), B.cuda()
+    for _ in range(3):
+        c = torch.full((M, 1024), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+        assert plan.check()[0] == 0
+        _assert_bit_exact(A, B, "f16", c.cpu())
+    plan.close()
+
+
+@pytest.mark.parametrize("shape", [(700, 1000, 520), (300, 900, 136), (1000, 777, 64)])
+def test_tail_split_ragged_edges(shape):
+    # Narrow tail tiles that straddle or lie beyond the last column / row.
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, seed=M + N + K)
+    for cg in (1, 2):
+        C, info, canary = gu.run_device(A, B, "f16", cta_group=cg, tile_n=256, max_ctas=3 * cg,
+                                        tail_split=4)
+        st, _, _ = gu.check_full(A, B, "f16", C)
+        assert canary and st["ok"], (shape, cg, st, info)
+
+
+def test_tail_split_gelu_bf16():
+    A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=512, N=1536, K=2048)
+    C1, i1, _ = gu.run_device(A, B, "bf16", epilogue="gelu", cta_group=2, max_ctas=10,
+                              tail_split=4)
+    assert i1["tail_splits"] == 4 and i1["tail_tiles"] > 0
+    st, _, _ = gu.check_full(A, B, "bf16", C1, epilogue="gelu")
+    assert st["ok"], st
+
+
+def test_tail_split_invalid_width_rejected():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    with pytest.raises(sg.GemmError) as ei:
+        sg.Plan(768, 1024, 1024, "f16", cta_group=2, tile_n=256, max_ctas=10, tail_split=3)
+    assert ei.value.status == sg.GEMM_ERR_INVALID_ARG
+
+
+def test_auto_tail_split_choice():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    # 8192^3: 1024 pair tiles over 76 clusters leave a last wave 47 % full: no cut.
+    p = sg.Plan(8192, 8192, 8192, "f16", stages=6)
+    info = p.info()
+    p.close()
+    assert info["cta_group"] == 2 and info["tail_splits"] == 1
+    # GELU layer: 768 pair tiles leave 8 over: cut 4 ways into 256 x 64 tiles.
+    p = sg.Plan(3072, 16384, 4096, "bf16", "gelu", stages=6)
+    info = p.info()
+    p.close()
+    walkers = info["grid"] // info["cta_group"]
+    if info["num_tiles"] % walkers * 4 <= walkers:
+        assert info["tail_splits"] == 4 and info["tail_tiles"] == info["num_tiles"] % walkers
+
+
+@pytest.mark.parametrize("shape", [(64, 2048, 1024), (100, 4096, 576), (128, 1000, 200)])
+def test_single_tile_row_rotated_k_bit_exact(shape):
+    # One row of tiles: each CTA starts its K loop at a different slice.
+    M, N, K = shape
+    A, B = _int_inputs(M, N, K, "f16", seed=M + N)
+    C, info, canary = gu.run_device(A, B, "f16")
+    assert canary and info["num_tiles"] > 1
+    _assert_bit_exact(A, B, "f16", C)
