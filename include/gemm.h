@@ -99,6 +99,10 @@ typedef struct {
                           {2, 3, 4} = cut each leftover tile along N into k narrower
                           tiles (>= 64 columns each, k must divide tile_n) */
   int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
+  int debug_fault;     /* test hook, 0 in normal use.  1: the first CTA's copy engine
+                          never receives its first K slice, so the pipeline's waits run
+                          out their time limit and gemm_plan_check reports
+                          GEMM_ERR_TIMEOUT (every other tile still completes) */
 } gemm_tuning_t;
 
 /* Read-only description of what a plan will launch (for tests and benchmarks). */

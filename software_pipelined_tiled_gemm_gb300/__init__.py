@@ -56,7 +56,8 @@ GEMM_SINGLE_BUFFER = 1
 class GemmTuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
-                ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64)]
+                ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
+                ("debug_fault", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -233,7 +234,7 @@ class Plan:
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
                  tile_n=0, raster_group=0, max_ctas=0, cta_group=0, tail_split=0,
-                 timeout_ns=0):
+                 timeout_ns=0, debug_fault=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -242,7 +243,7 @@ class Plan:
         self.device = int(device)
         self._h = None
         tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
-                            int(tail_split), int(timeout_ns))
+                            int(tail_split), int(timeout_ns), int(debug_fault))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")

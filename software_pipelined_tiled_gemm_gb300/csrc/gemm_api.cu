@@ -109,6 +109,7 @@ struct gemm_plan {
   int64_t tiles_m = 0, tiles_n = 0, num_tiles = 0;
   size_t smem = 0;
   unsigned long long timeout_ns = kDefaultTimeoutNs;
+  int debug_fault = 0;
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -258,6 +259,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     if (want_group < 0 || want_ctas < 0)
       return fail(GEMM_ERR_INVALID_ARG, "negative raster_group / max_ctas");
     if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
+    if (tuning->debug_fault < 0 || tuning->debug_fault > 1)
+      return fail(GEMM_ERR_INVALID_ARG, "debug_fault %d not in {0, 1}", tuning->debug_fault);
     if (tuning->timeout_ns > 0) timeout = static_cast<unsigned long long>(tuning->timeout_ns);
   }
 
@@ -340,6 +343,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->timeout_ns = timeout;
   p->num_acc = variant == GEMM_SINGLE_BUFFER ? 1 : 2;
   p->max_ctas = want_ctas;
+  p->debug_fault = tuning ? tuning->debug_fault : 0;
   p->bn = chosen;
   p->cg = chosen_cg;
   p->smem = chosen_smem;
@@ -562,6 +566,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   // One row of tiles across the whole grid: every CTA reads the same A rows,
   // so stagger where each starts along K.
   prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
+  prm.inject_fault = plan->debug_fault;
 
   cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC, prm,
                          plan->grid, plan->smem, stream);

@@ -234,17 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t sa = sbase + stage * kStage;
+          // Test hook: the first slice of CTA 0 is announced but never copied.
+          const bool skip = p.inject_fault && blockIdx.x == 0 && u == unit && i == 0;
           if constexpr (CG == 2) {
             // Both CTAs' copies count on the leader's full barrier; only the
             // leader announces the bytes (of both CTAs).
             const uint32_t fb = ptx::map_shared_rank(full_bar(stage), 0);
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-            ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-            ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
+            if (!skip) {
+              ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
+              ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
+            }
           } else {
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-            ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-            ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
+            if (!skip) {
+              ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
+              ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
+            }
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);

@@ -63,6 +63,9 @@ struct Params {
   // so CTAs that share the same A rows do not all read the same A slice at
   // the same time (used when a single row of tiles spans the whole grid).
   int k_rotate;
+  // Test hook: 1 = the producer of CTA 0 announces but never issues the
+  // copies of its first K slice (see gemm_tuning_t::debug_fault).
+  int inject_fault;
 };
 
 // Shared memory a CTA needs for a given tile width / ring depth / staging;
