@@ -46,7 +46,7 @@ def log(*a):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gemm_8192_f16", choices=sorted(gemm_inputs.WORKLOADS))
@@ -110,16 +110,19 @@ def traffic_from_profiles(workload, digest):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
+    """nvidia-smi clock/throttle samples, kept only when they fall inside the
+    timed region (host wall-clock window marked with mark_start/mark_stop)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.tmp = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -128,14 +131,28 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.tmp, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            time.sleep(0.5)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _parse_ts(text):
+        # "YYYY/MM/DD HH:MM:SS.mmm", local time of this host
+        text = text.strip()
+        main, _, frac = text.partition(".")
+        t = time.mktime(time.strptime(main, "%Y/%m/%d %H:%M:%S"))
+        return t + (float("0." + frac) if frac else 0.0)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.2)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -143,26 +160,47 @@ class ClockSampler:
             self.proc.kill()
         self.tmp.flush()
         self.tmp.seek(0)
-        rows = [r.strip().split(",") for r in self.tmp.read().splitlines() if r.strip()]
+        rows = [r.split(",") for r in self.tmp.read().splitlines() if r.strip()]
         os.unlink(self.tmp.name)
-        sm, mx, pw, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for r in rows:
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-                pw.append(float(r[3]))
+                ts = self._parse_ts(r[0])
+                samples.append((ts, float(r[2]), float(r[3]), float(r[4]),
+                                [n for i, n in enumerate(self.REASONS)
+                                 if len(r) > 6 + i and r[6 + i].strip().lower() == "active"]))
             except (ValueError, IndexError):
                 continue
-            for i, n in enumerate(names):
-                if len(r) > 5 + i and r[5 + i].strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [s for s, p in zip(sm, pw) if p > 0.5 * max(pw)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(pw) if pw else None}
+        inside = [x for x in samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            mid = (self.t0 + self.t1) / 2 if self.t0 is not None else samples[-1][0]
+            inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
+            window = "nearest to the timed region"
+        reasons = sorted({n for x in inside for n in x[4]})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in samples),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(x[3] for x in inside)}
+
+
+def reduce_max(value, world_size, device=None):
+    """Largest `value` over all ranks (the slowest rank decides the job time)."""
+    if world_size <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step, steps, world_size, elapsed_ms):
+    """Whole-job TFLOP/s: every rank's steps over the slowest rank's time."""
+    return flops_per_step * steps * world_size / (elapsed_ms * 1e-3) / 1e12
 
 
 def cpu_baseline(A, B, w, seconds, threads=0):
@@ -277,6 +315,7 @@ def main():
     clocks.start()
     barrier()
     torch.cuda.synchronize(dev)
+    clocks.mark_start()
     ev0.record(stream)
     for i in range(args.steps):
         ks[i].record(stream)
@@ -284,6 +323,7 @@ def main():
         ke[i].record(stream)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark_stop()
     barrier()
     clk = clocks.stop()
     elapsed_ms = ev0.elapsed_time(ev1)
@@ -291,13 +331,10 @@ def main():
     ds, detail = plan.check()
     if ds != 0:
         raise SystemExit("device status %d (detail %#x) after timed steps" % (ds, detail))
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(elapsed_ms, ws, dev)
 
     flops = 2.0 * w.M * w.N * w.K
-    value = flops * args.steps * ws / (elapsed_ms * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, ws, elapsed_ms)
     kavg = sum(kern_ms) / len(kern_ms)
     achieved = flops / (kavg * 1e-3) / 1e12
 
@@ -314,13 +351,9 @@ def main():
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
-        el = time.perf_counter() - t0
-        if ws > 1:
-            t = torch.tensor([el], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
+        el = reduce_max(time.perf_counter() - t0, ws, dev)
         eplan.close()
-        e2e = {"value": flops * args.e2e_steps * ws / el / 1e12, "unit": UNIT,
+        e2e = {"value": job_throughput(flops, args.e2e_steps, ws, el * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": (w.M * w.K + w.N * w.K) * 2,
                "d2h_bytes_per_step": w.M * w.N * 2}
 

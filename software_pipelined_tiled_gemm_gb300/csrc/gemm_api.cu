@@ -8,6 +8,7 @@
 // bytes this kernel adds on top.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdarg>
@@ -461,6 +462,11 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   DeviceGuard guard(plan->device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_handle);
+  // Host-side range for profilers and tracers (a no-op without one attached).
+  struct NvtxRange {
+    NvtxRange() { nvtxRangePushA("gemm_run"); }
+    ~NvtxRange() { nvtxRangePop(); }
+  } nvtx_range;
 
   if (K == 0) {  // empty reduction: C = 0, and GELU(0) = 0
     cudaError_t e = cudaMemsetAsync(C, 0, bytesC, stream);

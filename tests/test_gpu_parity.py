@@ -426,3 +426,22 @@ def test_single_tile_row_rotated_k_bit_exact(shape):
     C, info, canary = gu.run_device(A, B, "f16")
     assert canary and info["num_tiles"] > 1
     _assert_bit_exact(A, B, "f16", C)
+
+
+def test_hundred_runs_bit_identical():
+    # Race check: a stale ring slot or accumulator would show up as a
+    # changed bit somewhere in 100 repetitions of the same GEMM.
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = gemm_inputs.custom(1024, 1024, 2048, dist="normal_scaled", seed=99)
+    a, b = A.cuda(), B.cuda()
+    plan = sg.Plan(1024, 1024, 2048, "f16", stages=6)
+    outs = torch.empty(100, 1024, 1024, dtype=torch.float16, device="cuda")
+    for i in range(100):
+        plan.run(a, b, outs[i])
+    torch.cuda.synchronize()
+    assert plan.check()[0] == 0
+    plan.close()
+    first = outs[0].view(torch.int16)
+    assert all(torch.equal(first, outs[i].view(torch.int16)) for i in range(1, 100))
+    st, _, _ = gu.check_full(A, B, "f16", outs[0].cpu())
+    assert st["ok"], st
