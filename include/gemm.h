@@ -95,9 +95,12 @@ typedef struct {
   int cta_group;       /* CTAs per output tile: 0 (auto), 1 (128-row tiles), or 2
                           (a CTA pair on two SMs computes a 256-row tile with
                           cta_group::2 MMAs; tile_n then 128 or 256) */
-  int tail_split;      /* the last, partial wave of tiles: 0 = auto, -1 = off, k in
-                          {2, 3, 4} = cut each leftover tile along N into k narrower
-                          tiles (>= 64 columns each, k must divide tile_n) */
+  int tail_split;      /* the last, partial wave of tiles: 0 = auto, -1 = off,
+                          1 = stream-K (the last one to two waves' K iterations are
+                          shared out evenly; a tile split between two CTAs is summed
+                          in a fixed order, so results are deterministic),
+                          k in {2, 3, 4} = cut each leftover tile along N into k
+                          narrower tiles (>= 64 columns each, k must divide tile_n) */
   int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
   int debug_fault;     /* test hook, 0 in normal use.  1: the first CTA's copy engine
                           never receives its first K slice, so the pipeline's waits run
@@ -122,6 +125,7 @@ typedef struct {
   int64_t tail_tiles;          /* tiles of the last wave that are cut into narrow tiles */
   int tail_splits;             /* narrow tiles per cut tile (1 = none) */
   int64_t work_units;          /* whole tiles + narrow tiles walked by the CTAs */
+  int stream_k;                /* 1: the tail_tiles are shared out stream-K */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

@@ -68,7 +68,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("pads_operands", ctypes.c_int), ("tma_store", ctypes.c_int),
                 ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("cta_group", ctypes.c_int), ("tail_tiles", ctypes.c_int64),
-                ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64)]
+                ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64),
+                ("stream_k", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -116,6 +116,9 @@ struct gemm_plan {
   int64_t dp_tiles = 0;          // tiles run whole
   int tail_splits = 1;           // narrow tiles per tail tile (cut along N)
   int64_t num_units = 0;
+  int64_t sk_tiles = 0;          // stream-K tiles after dp_tiles
+  float* sk_ws = nullptr;        // fp32 partials of stream-K tiles
+  int* sk_flags = nullptr;       // partial-ready flags (reset by the owner)
   uint16_t* scratch = nullptr;   // padded copies of A and/or B
   size_t scratch_bytes = 0;
 
@@ -249,8 +252,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     want_ctas = tuning->max_ctas;
     want_cg = tuning->cta_group;
     want_split = tuning->tail_split;
-    if (want_split < -1 || want_split == 1 || want_split > kMaxTailSplits)
-      return fail(GEMM_ERR_INVALID_ARG, "tail_split %d not in {-1, 0, 2, 3, 4}", want_split);
+    if (want_split < -1 || want_split > kMaxTailSplits)
+      return fail(GEMM_ERR_INVALID_ARG, "tail_split %d not in {-1, 0, 1, 2, 3, 4}", want_split);
     if (want_bn != 0 && want_bn != 64 && want_bn != 128 && want_bn != 256)
       return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", want_bn);
     if (want_cg < 0 || want_cg > 2)
@@ -368,19 +371,39 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     walkers = p->sm_count;
     if (want_ctas > 0) walkers = std::min(walkers, want_ctas);
   }
-  // Cut the tiles of the last, partial wave along N into narrower tiles
-  // (at least 64 columns each) so that wave keeps more walkers busy for a
-  // shorter time.  No reduction is needed: the narrow tiles are disjoint.
-  // Narrow MMAs re-read A from shared memory for fewer columns, so the
-  // automatic choice only cuts a last wave that is at most a quarter full
-  // (measured on GB300: a 4-way cut of 8 leftover 256x256 tiles gains ~3 %,
-  // 2-way cuts of waves a third to half full lose 2 %).
+  // The last, partial wave.  Stream-K: leave (full waves - 1) waves of
+  // whole tiles and share the K iterations of the remaining one to two
+  // waves' tiles evenly among all walkers; each walker then holds at least
+  // one tile's worth, so a tile is split between at most two walkers and the
+  // owner (holding K slice 0, processed last) adds one partial.  The owner
+  // stages that partial in its idle ring, which must hold 4 x 32 x BN fp32.
+  // Narrow tiles: cut the leftover tiles along N (>= 64 columns each); no
+  // reduction, but narrow MMAs re-read A for fewer columns, so automatic
+  // mode uses them only when stream-K does not apply and the wave is at
+  // most a quarter full.
+  const int64_t k_blocks = cdiv(K, kBK);
   p->dp_tiles = p->num_tiles;
   p->tail_splits = 1;
+  p->sk_tiles = 0;
   if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
     const int64_t rem = p->num_tiles % walkers;
+    const int64_t ring = static_cast<int64_t>(stages) *
+                         (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
+    const bool sk_fits = ring >= static_cast<int64_t>(kEpiWarps) * 32 * p->bn * 4;
+    const bool sk_ok = rem > 0 && p->num_tiles >= walkers && sk_fits && k_blocks >= 2;
     const int max_s = std::min(kMaxTailSplits, p->bn / kStoreCols);
-    if (rem > 0 && (want_split >= 2 || rem * 4 <= walkers)) {
+    if (want_split == 1 || (want_split == 0 && sk_ok)) {
+      if (!sk_ok && want_split == 1 && rem > 0) {
+        delete p;
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "stream-K needs at least one full wave of tiles and a ring of >= %d B",
+                    kEpiWarps * 32 * p->bn * 4);
+      }
+      if (sk_ok) {
+        p->dp_tiles = (p->num_tiles / walkers - 1) * walkers;
+        p->sk_tiles = p->num_tiles - p->dp_tiles;
+      }
+    } else if (rem > 0 && (want_split >= 2 || rem * 4 <= walkers)) {
       int64_t S = want_split >= 2 ? want_split : std::min<int64_t>(walkers / rem, max_s);
       if (S >= 2 && S <= max_s && p->bn % S == 0) {
         p->dp_tiles = p->num_tiles - rem;
@@ -394,12 +417,13 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     }
   }
   const int64_t tail = p->num_tiles - p->dp_tiles;
-  p->num_units = p->dp_tiles + tail * p->tail_splits;
+  p->num_units = p->sk_tiles > 0 ? p->dp_tiles : p->dp_tiles + tail * p->tail_splits;
   if (p->num_units > kMaxDim) {
     delete p;
     return fail(GEMM_ERR_INVALID_ARG, "too many work units");
   }
-  p->grid = chosen_cg * static_cast<int>(std::min<int64_t>(p->num_units, walkers));
+  p->grid = chosen_cg * static_cast<int>(
+                           std::min<int64_t>(p->sk_tiles > 0 ? walkers : p->num_units, walkers));
 
   // The limit is per kernel function, shared by every plan on the device:
   // always raise it to the device maximum, never to this plan's own size, so
@@ -408,6 +432,17 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   if (e != cudaSuccess) {
     delete p;
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+  }
+  if (p->sk_tiles > 0) {
+    const size_t nflags = static_cast<size_t>(p->sk_tiles) * chosen_cg * kEpiWarps;
+    if ((e = cudaMalloc(&p->sk_ws, nflags * 32 * p->bn * sizeof(float))) != cudaSuccess ||
+        (e = cudaMalloc(&p->sk_flags, nflags * sizeof(int))) != cudaSuccess ||
+        (e = cudaMemset(p->sk_flags, 0, nflags * sizeof(int))) != cudaSuccess) {
+      if (p->sk_ws) cudaFree(p->sk_ws);
+      if (p->sk_flags) cudaFree(p->sk_flags);
+      delete p;
+      return cuda_fail(e, "cudaMalloc(stream-K workspace)");
+    }
   }
   e = cudaMalloc(&p->d_status, 4 * sizeof(int));
   if (e != cudaSuccess) {
@@ -573,6 +608,9 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   // so stagger where each starts along K.
   prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
   prm.inject_fault = plan->debug_fault;
+  prm.sk_tiles = static_cast<int>(plan->sk_tiles);
+  prm.sk_ws = plan->sk_ws;
+  prm.sk_flags = plan->sk_flags;
 
   cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC, prm,
                          plan->grid, plan->smem, stream);
@@ -632,6 +670,12 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
   if (e != cudaSuccess) return cuda_fail(e, "read status word");
   e = cudaMemset(plan->d_status, 0, sizeof(h));
   if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  if (h[0] != 0 && plan->sk_flags) {
+    // A launch that gave up part-way may have left partial-ready flags raised.
+    e = cudaMemset(plan->sk_flags, 0,
+                   static_cast<size_t>(plan->sk_tiles) * plan->cg * kEpiWarps * sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear stream-K flags");
+  }
   *device_status = h[0];
   if (detail) *detail = h[1];
   return GEMM_OK;
@@ -656,6 +700,8 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->tail_tiles = plan->num_tiles - plan->dp_tiles;
   info->tail_splits = plan->tail_splits;
   info->work_units = plan->num_units;
+  info->stream_k = plan->sk_tiles > 0 ? 1 : 0;
+  if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
   return GEMM_OK;
 }
 
@@ -666,6 +712,8 @@ void gemm_plan_destroy(gemm_plan_t* plan) {
     if (guard.err == cudaSuccess) {
       cudaDeviceSynchronize();
       if (plan->d_status) cudaFree(plan->d_status);
+      if (plan->sk_ws) cudaFree(plan->sk_ws);
+      if (plan->sk_flags) cudaFree(plan->sk_flags);
       if (plan->scratch) cudaFree(plan->scratch);
       if (plan->hA) cudaFree(plan->hA);
       if (plan->hB) cudaFree(plan->hB);

@@ -19,7 +19,7 @@
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,                   \
                                  const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid, size_t smem, \
                                  cudaStream_t stream) {                                        \
-    if (p.tail_splits > 1)                                                                     \
+    if (p.tail_splits > 1 || p.sk_tiles > 0)                                                                     \
       gemm_tn_kernel<BN, 1, true><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);               \
     else                                                                                       \
       gemm_tn_kernel<BN, 1, false><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);              \
@@ -64,7 +64,7 @@
     cudaLaunchConfig_t cfg;                                                                     \
     cudaLaunchAttribute attr[1];                                                                \
     pair_config_##BN(cfg, attr, grid, smem, stream);                                            \
-    if (p.tail_splits > 1)                                                                      \
+    if (p.tail_splits > 1 || p.sk_tiles > 0)                                                                      \
       return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, true>, a, b, bt, c, p);                 \
     return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, false>, a, b, bt, c, p);                  \
   }                                                                                             \

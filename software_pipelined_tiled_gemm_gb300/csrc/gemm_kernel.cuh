@@ -83,6 +83,27 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t pari
   }
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Wait (bounded) until another walker has raised *flag after publishing its
+// partial sum.
+__device__ __forceinline__ bool wait_flag(const int* flag, const Params& p, int detail) {
+  if (ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (ld_acquire_gpu(flag) == 0) {
+    __nanosleep(32);
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      record_error(p.status, kStatusTimeout, detail);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Grouped tile order: tiles are taken `raster_group` tile rows at a time,
 // column by column inside a group.
 __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int& nb) {
@@ -95,31 +116,80 @@ __device__ __forceinline__ void tile_coords(int t, const Params& p, int& mb, int
   nb = r / rows;
 }
 
-// Work unit -> (tile, sub-tile).  A tail tile is cut along N into
-// tail_splits narrow tiles; every other tile is one unit.
-__device__ __forceinline__ void unit_info(int u, const Params& p, int& tile, int& sub) {
-  if (u < p.dp_tiles) {
-    tile = u;
-    sub = -1;
-  } else {
-    const int v = u - p.dp_tiles;
-    tile = p.dp_tiles + v / p.tail_splits;
-    sub = v - (v / p.tail_splits) * p.tail_splits;
-  }
-}
+// One piece of work for a walker (a CTA, or a CTA pair).
+struct Unit {
+  int tile;    // raster index of the output tile
+  int sub;     // narrow tail tile index along N, or -1 for a full-width tile
+  int k0, k1;  // K slices [k0, k1) of this piece
+  int role;    // kWhole, kContrib (partial sum for another walker), kOwner (adds it, stores)
+  int seq;     // running count of this walker's units
+};
+constexpr int kWhole = 0, kContrib = 1, kOwner = 2;
 
-// First K slice of a unit's loop: 0, or spread over the K range by unit index.
-__device__ __forceinline__ int k_start(int u, int units, const Params& p) {
-  if (!p.k_rotate) return 0;
-  const int n = units < p.num_units ? units : p.num_units;
-  return static_cast<int>((static_cast<int64_t>(u % n) * p.k_blocks) / n);
+// Enumerates a walker's units: first its whole tiles (and narrow tail
+// tiles), walker, walker + walkers, ...; then, with stream-K, its contiguous
+// share [begin, end) of the remaining sk_tiles * k_blocks K iterations.
+struct UnitIter {
+  int u;
+  int walkers;
+  int seq = 0;
+  int64_t sk_it = 0, sk_end = 0;
+  __device__ UnitIter(int walker, int walkers_, const Params& p) : u(walker), walkers(walkers_) {
+    if (p.sk_tiles > 0) {
+      const int64_t total = static_cast<int64_t>(p.sk_tiles) * p.k_blocks;
+      sk_it = total * walker / walkers;
+      sk_end = total * (walker + 1) / walkers;
+    }
+  }
+  __device__ bool next(const Params& p, Unit& x) {
+    if (u < p.num_units) {
+      if (u < p.dp_tiles) {
+        x.tile = u;
+        x.sub = -1;
+      } else {
+        const int v = u - p.dp_tiles;
+        x.tile = p.dp_tiles + v / p.tail_splits;
+        x.sub = v - (v / p.tail_splits) * p.tail_splits;
+      }
+      x.k0 = 0;
+      x.k1 = p.k_blocks;
+      x.role = kWhole;
+      x.seq = seq++;
+      u += walkers;
+      return true;
+    }
+    if (sk_it < sk_end) {
+      const int64_t tl = sk_it / p.k_blocks;
+      x.tile = p.dp_tiles + static_cast<int>(tl);
+      x.sub = -1;
+      x.k0 = static_cast<int>(sk_it - tl * p.k_blocks);
+      const int64_t left = sk_end - sk_it;
+      x.k1 = static_cast<int>(x.k0 + left < p.k_blocks ? x.k0 + left : p.k_blocks);
+      x.role = (x.k0 == 0 && x.k1 == p.k_blocks) ? kWhole : (x.k0 > 0 ? kContrib : kOwner);
+      x.seq = seq++;
+      sk_it += x.k1 - x.k0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// First K slice of a whole unit's loop: 0, or spread over the K range.
+__device__ __forceinline__ int k_start(const Unit& x, int walker, int walkers, const Params& p) {
+  if (!p.k_rotate || x.role != kWhole) return 0;
+  const int n = walkers < p.num_units ? walkers : p.num_units;
+  const int idx = (walker + x.seq * walkers) % n;
+  return static_cast<int>((static_cast<int64_t>(idx) * p.k_blocks) / n);
 }
 
 __device__ __forceinline__ float gelu_tanh(float x) {
-  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)); this form cannot produce
-  // inf/inf for large |u| (x -> x for u -> +inf, x -> -0 for u -> -inf).
-  const float u = 0.7978845608f * (x + 0.044715f * x * x * x);
-  return x / (1.0f + __expf(-2.0f * u));
+  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)), u = 0.7978845608 (x + 0.044715 x^3);
+  // this form cannot produce inf/inf for large |u| (x -> x for u -> +inf,
+  // x -> -0 for u -> -inf).  CUDA's fast exponential and division keep the
+  // epilogue cheap; their few-ulp fp32 error is far below the 8/11-bit
+  // precision of the rounded output, and __fdividef(x, inf) gives -0/+0.
+  const float inner = x * fmaf(0.044715f, x * x, 1.0f);
+  return __fdividef(x, 1.0f + __expf(-1.5957691216f * inner));
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
@@ -136,8 +206,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 // rows of A and BN/2 rows of B, the even CTA issues the MMAs for both, and
 // each CTA's TMEM receives its own 128 rows of the accumulator).
 // kSplit: this instance can run narrow tail tiles (BN / tail_splits wide,
-// B loaded through tmBt); the instance used by plans without a tail split
-// has that code compiled out.
+// B loaded through tmBt) and stream-K pieces; the instance used by plans
+// that need neither has that code compiled out.
 template <int BN, int CG, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -148,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kStageB = kBRows * kBK * 2;
   constexpr uint32_t kStage = kStageA + kStageB;     // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
+  constexpr uint32_t kWarpPartial = 32u * BN * 4u;   // fp32 partial of one epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B
@@ -166,8 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + a); };
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + 2 + a); };
   const uint32_t done_bar = bar_base + 8u * (2 * kMaxStages + 4);
+  auto fix_bar = [&](int q) { return bar_base + 8u * (2 * kMaxStages + 5 + q); };
   uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 5));
+      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 9));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Position in the CTA pair (always 0 without one).
   const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
   const bool leader = rank == 0;
-  const int unit = static_cast<int>(blockIdx.x) / CG;      // tile walker id
-  const int units = static_cast<int>(gridDim.x) / CG;
+  const int walker = static_cast<int>(blockIdx.x) / CG;
+  const int walkers = static_cast<int>(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -189,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty_bar(a), kEpiWarps * CG);
     }
     ptx::mbar_init(done_bar, 1);
+    for (int q = 0; q < kEpiWarps; ++q) ptx::mbar_init(fix_bar(q), 1);
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -216,26 +289,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-slot: used at all / parity of last use
       bool ok = true;
-      for (int u = unit; ok && u < p.num_units; u += units) {
-        int t, sub, mb, nb;
-        unit_info(u, p, t, sub);
-        tile_coords(t, p, mb, nb);
-        const bool narrow = kSplit && sub >= 0;
+      UnitIter it(walker, walkers, p);
+      Unit x;
+      while (ok && it.next(p, x)) {
+        int mb, nb;
+        tile_coords(x.tile, p, mb, nb);
+        const bool narrow = kSplit && x.sub >= 0;
         const int n_width = narrow ? BN / p.tail_splits : BN;   // columns of this unit
         const int b_rows = n_width / CG;                        // B rows this CTA loads
         const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
-        const int b_row = nb * BN + (narrow ? sub * n_width : 0) + static_cast<int>(rank) * b_rows;
+        const int b_row = nb * BN + (narrow ? x.sub * n_width : 0) + static_cast<int>(rank) * b_rows;
         const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
         const uint32_t bytes = (kStageA + static_cast<uint32_t>(b_rows) * kBK * 2u) * CG;
-        const int k0 = k_start(u, units, p);
-        for (int i = 0, kb = k0; i < p.k_blocks; ++i, kb = (kb + 1 == p.k_blocks) ? 0 : kb + 1) {
+        const int nk = x.k1 - x.k0;
+        const int kr = k_start(x, walker, walkers, p);
+        for (int i = 0, kb = x.k0 + kr; i < nk; ++i, kb = (kb + 1 == x.k1) ? x.k0 : kb + 1) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
             ok = false;
             break;
           }
           const uint32_t sa = sbase + stage * kStage;
           // Test hook: the first slice of CTA 0 is announced but never copied.
-          const bool skip = p.inject_fault && blockIdx.x == 0 && u == unit && i == 0;
+          const bool skip = p.inject_fault && blockIdx.x == 0 && x.seq == 0 && i == 0;
           if constexpr (CG == 2) {
             // Both CTAs' copies count on the leader's full barrier; only the
             // leader announces the bytes (of both CTAs).
@@ -278,15 +353,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = unit; ok && u < p.num_units; u += units) {
-        int t, sub;
-        unit_info(u, p, t, sub);
-        const uint32_t idesc = (kSplit && sub >= 0) ? p.idesc_tail : p.idesc;
+      UnitIter it(walker, walkers, p);
+      Unit x;
+      while (ok && it.next(p, x)) {
+        const uint32_t idesc = (kSplit && x.sub >= 0) ? p.idesc_tail : p.idesc;
         if (!wait_bounded_cluster<CG>(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty))
           break;
         ptx::tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {  // iteration count (slices may be rotated)
+        const int nk = x.k1 - x.k0;
+        for (int kb = 0; kb < nk; ++kb) {  // iteration count (slices may be rotated)
           if (!wait_bounded(full_bar(stage), phase, p, kDetailMmaFull)) {
             ok = false;
             break;
@@ -333,15 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* my_stage = staging + ew * p.store_bufs * kStoreBuf;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t fix_phase = 0;
     int buf = 0;
     const bool bf16 = p.bf16 != 0;
-    for (int u = unit; u < p.num_units; u += units) {
-      int t, sub, mb, nb;
-      unit_info(u, p, t, sub);
-      tile_coords(t, p, mb, nb);
-      const bool narrow = kSplit && sub >= 0;
+    UnitIter it(walker, walkers, p);
+    Unit x;
+    while (it.next(p, x)) {
+      int mb, nb;
+      tile_coords(x.tile, p, mb, nb);
+      const bool narrow = kSplit && x.sub >= 0;
       const int n_width = narrow ? BN / p.tail_splits : BN;
-      const int n0 = nb * BN + (narrow ? sub * n_width : 0);
+      const int n0 = nb * BN + (narrow ? x.sub * n_width : 0);
       const uint32_t chunks = static_cast<uint32_t>(n_width) / kStoreCols;
       int ready = 1;
       if (lane == 0) ready = wait_bounded(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
@@ -352,7 +430,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row0 = mb * kTileM + static_cast<int>(rank) * kBM + q * 32;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
-      if (row0 < p.M) {
+      // Stream-K: this warp's fp32 partial of a shared tile, laid out
+      // [column][lane] (one coalesced 128-byte line per column).
+      const uint32_t flag_idx =
+          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * kEpiWarps + q;
+      float* partial = (kSplit && x.role != kWhole)
+                           ? p.sk_ws + static_cast<size_t>(flag_idx) * (kWarpPartial / 4u)
+                           : nullptr;
+      bool have_partial = false;
+      if (kSplit && x.role == kContrib) {
+        // Publish the partial sum of K slices [k0, k1) and raise the flag.
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_row + c, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) __stcg(partial + (c + j) * 32 + lane, __uint_as_float(v[j]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.sk_flags + flag_idx, 1);
+      } else if (kSplit && x.role == kOwner) {
+        // The other walker's partial (K slices [k1, k_blocks)) was written at
+        // the start of its range.  This is the last unit of this walker, so
+        // the ring is idle: bulk-copy the partial into it.
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_flag(p.sk_flags + flag_idx, p, kDetailSkFlag) ? 1 : 0;
+          if (ok) {
+            p.sk_flags[flag_idx] = 0;  // ready for the next launch
+            ptx::mbar_arrive_expect_tx(fix_bar(q), kWarpPartial);
+            ptx::bulk_load(sbase + q * kWarpPartial, partial, kWarpPartial, fix_bar(q));
+            ok = wait_bounded(fix_bar(q), fix_phase, p, kDetailSkCopy) ? 1 : 0;
+          }
+        }
+        fix_phase ^= 1u;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        have_partial = ok != 0;
+        if (!have_partial) break;
+      }
+      if ((!kSplit || x.role != kContrib) && row0 < p.M) {
+        const float* fix = reinterpret_cast<const float*>(smem + q * kWarpPartial);
 #pragma unroll 1
         for (uint32_t c = 0; c < chunks; ++c) {
           const int col0 = n0 + static_cast<int>(c) * kStoreCols;
@@ -361,6 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols, r0);
           ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols + 32, r1);
           ptx::tmem_wait_ld();
+          if (kSplit && have_partial) {
+            // own slices first, then the partial: a fixed order on every run
+            const int cb = static_cast<int>(c) * kStoreCols;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              r0[j] = __float_as_uint(__uint_as_float(r0[j]) + fix[(cb + j) * 32 + lane]);
+              r1[j] = __float_as_uint(__uint_as_float(r1[j]) + fix[(cb + 32 + j) * 32 + lane]);
+            }
+          }
           uint32_t pk[32];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -425,9 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int h = 0; h < 2; ++h) {
                 const int cc = lane + 32 * h;
                 if (cc < ncols) {
-                  const uint32_t off = static_cast<uint32_t>(r) * 128u +
-                                       ((static_cast<uint32_t>(cc >> 3) ^ (static_cast<uint32_t>(r) & 7u)) << 4) +
-                                       static_cast<uint32_t>(cc & 7) * 2u;
+                  const uint32_t off =
+                      static_cast<uint32_t>(r) * 128u +
+                      ((static_cast<uint32_t>(cc >> 3) ^ (static_cast<uint32_t>(r) & 7u)) << 4) +
+                      static_cast<uint32_t>(cc & 7) * 2u;
                   crow[cc] = *reinterpret_cast<const uint16_t*>(sb + off);
                 }
               }

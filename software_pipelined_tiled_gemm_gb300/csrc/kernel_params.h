@@ -16,7 +16,7 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kStageA = kBM * kBK * 2;             // 16 KiB
 constexpr int kStoreCols = 64;                          // epilogue step: 64 columns
 constexpr uint32_t kStoreBuf = 32u * kStoreCols * 2u;   // 32 rows x 128 B = 4 KiB
-constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 5) + 16u;
+constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 9) + 16u;
 constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
@@ -30,6 +30,8 @@ constexpr int kDetailMmaAccEmpty = (2 << 16) | 1;
 constexpr int kDetailMmaFull = (2 << 16) | 2;
 constexpr int kDetailMmaDrain = (2 << 16) | 3;
 constexpr int kDetailEpiFull = (3 << 16) | 1;
+constexpr int kDetailSkFlag = (3 << 16) | 2;
+constexpr int kDetailSkCopy = (3 << 16) | 3;
 
 struct Params {
   int M, N;              // output extent
@@ -59,6 +61,15 @@ struct Params {
   int tail_splits;
   int num_units;
   uint32_t idesc_tail;
+  // Stream-K (sk_tiles > 0): after the dp_tiles whole tiles, the remaining
+  // sk_tiles * k_blocks K iterations are shared out in contiguous ranges, one
+  // per walker (at least one tile's worth each, so a tile spans at most two
+  // walkers).  The walker holding a tile's first K slices owns it: the other
+  // writes its fp32 partial to sk_ws and raises sk_flags; the owner adds it
+  // and stores.  Mutually exclusive with tail_splits > 1.
+  int sk_tiles;
+  float* sk_ws;
+  int* sk_flags;
   // 1: each unit starts its K loop at a different slice (wrapping around),
   // so CTAs that share the same A rows do not all read the same A slice at
   // the same time (used when a single row of tiles spans the whole grid).

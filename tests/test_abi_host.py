@@ -75,7 +75,7 @@ def test_plan_create_ex_rejects_bad_tuning():
     for t in (sg.GemmTuning(96, 0, 0, 0, 0, 0), sg.GemmTuning(0, -1, 0, 0, 0, 0),
               sg.GemmTuning(0, 0, -2, 0, 0, 0), sg.GemmTuning(0, 0, 0, 3, 0, 0),
               sg.GemmTuning(0, 0, 0, -1, 0, 0), sg.GemmTuning(64, 0, 0, 2, 0, 0),
-              sg.GemmTuning(0, 0, 0, 0, 1, 0), sg.GemmTuning(0, 0, 0, 0, -2, 0),
+              sg.GemmTuning(0, 0, 0, 0, -2, 0),
               sg.GemmTuning(0, 0, 0, 0, 5, 0), sg.GemmTuning(0, 0, 0, 0, 0, -5),
               sg.GemmTuning(0, 0, 0, 0, 0, 0, 2)):
         st, h = sg.gemm_plan_create_ex(64, 64, 64, 0, 0, 4, 0, 0, t)

@@ -404,18 +404,67 @@ def test_tail_split_invalid_width_rejected():
 
 def test_auto_tail_split_choice():
     import software_pipelined_tiled_gemm_gb300 as sg
-    # 8192^3: 1024 pair tiles over 76 clusters leave a last wave 47 % full: no cut.
+    # 8192^3: 1024 pair tiles over 76 clusters: 12 whole waves, the K
+    # iterations of the last 112 tiles shared out stream-K.
     p = sg.Plan(8192, 8192, 8192, "f16", stages=6)
     info = p.info()
     p.close()
-    assert info["cta_group"] == 2 and info["tail_splits"] == 1
-    # GELU layer: 768 pair tiles leave 8 over: cut 4 ways into 256 x 64 tiles.
-    p = sg.Plan(3072, 16384, 4096, "bf16", "gelu", stages=6)
-    info = p.info()
-    p.close()
     walkers = info["grid"] // info["cta_group"]
-    if info["num_tiles"] % walkers * 4 <= walkers:
-        assert info["tail_splits"] == 4 and info["tail_tiles"] == info["num_tiles"] % walkers
+    assert info["cta_group"] == 2 and info["stream_k"] == 1
+    assert info["tail_tiles"] == info["num_tiles"] - (info["num_tiles"] // walkers - 1) * walkers
+    # a single-buffer plan never splits
+    p = sg.Plan(8192, 8192, 8192, "f16", stages=1, variant="single_buffer")
+    assert p.info()["stream_k"] == 0 and p.info()["tail_splits"] == 1
+    p.close()
+
+
+# ------------------------------------------------------------ stream-K --
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_stream_k_bit_exact_and_reusable(cta_group):
+    # 12 tiles over 5 walkers: 5 whole tiles, then the 7 x 16 K iterations of
+    # the other 7 tiles shared out (22-23 per walker), so 4-5 tiles are split
+    # between two walkers.  Three runs of the same plan: flags must reset.
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M = 768 if cta_group == 2 else 384
+    A, B = _int_inputs(M, 1024, 1024, "f16", seed=400 + cta_group)
+    plan = sg.Plan(M, 1024, 1024, "f16", stages=4, cta_group=cta_group, tile_n=256,
+                   max_ctas=5 * cta_group, tail_split=1)
+    info = plan.info()
+    assert info["stream_k"] == 1 and info["tail_tiles"] == 7 and info["grid"] == 5 * cta_group
+    a, b = A.cuda(), B.cuda()
+    for _ in range(3):
+        c = torch.full((M, 1024), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+        assert plan.check()[0] == 0
+        _assert_bit_exact(A, B, "f16", c.cpu())
+    plan.close()
+
+
+@pytest.mark.parametrize("shape", [(700, 1000, 520), (1000, 777, 264), (513, 1290, 1000)])
+def test_stream_k_ragged_edges(shape):
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, seed=M + 2 * N + K)
+    for cg in (1, 2):
+        C, info, canary = gu.run_device(A, B, "f16", cta_group=cg, tile_n=256, max_ctas=7 * cg,
+                                        tail_split=1)
+        st, _, _ = gu.check_full(A, B, "f16", C)
+        assert info["stream_k"] == 1, info
+        assert canary and st["ok"], (shape, cg, st, info)
+
+
+def test_stream_k_gelu_bf16_and_deterministic():
+    A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=512, N=1536, K=2048)
+    outs = []
+    for _ in range(2):
+        C, info, _ = gu.run_device(A, B, "bf16", epilogue="gelu", cta_group=2, max_ctas=10,
+                                   tail_split=1)
+        assert info["stream_k"] == 1
+        outs.append(C)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    st, _, _ = gu.check_full(A, B, "bf16", outs[0], epilogue="gelu")
+    assert st["ok"], st
 
 
 @pytest.mark.parametrize("shape", [(64, 2048, 1024), (100, 4096, 576), (128, 1000, 200)])
