@@ -17,13 +17,21 @@
                                 static_cast<int>(smem));                                       \
   }                                                                                            \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,                   \
-                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid, size_t smem, \
-                                 cudaStream_t stream) {                                        \
-    if (p.tail_splits > 1 || p.sk_tiles > 0)                                                                     \
-      gemm_tn_kernel<BN, 1, true><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);               \
-    else                                                                                       \
-      gemm_tn_kernel<BN, 1, false><<<grid, kThreads, smem, stream>>>(a, b, bt, c, p);              \
-    return cudaGetLastError();                                                                 \
+                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, \
+                                 int grid, size_t smem, cudaStream_t stream) {                 \
+    cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};                                             \
+    cudaLaunchAttribute attr[1];                                                               \
+    cfg.gridDim = dim3(grid, 1, 1);                                                            \
+    cfg.blockDim = dim3(kThreads, 1, 1);                                                       \
+    cfg.dynamicSmemBytes = smem;                                                               \
+    cfg.stream = stream;                                                                       \
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                           \
+    attr[0].val.programmaticStreamSerializationAllowed = 1;                                    \
+    cfg.attrs = attr;                                                                          \
+    cfg.numAttrs = 1;                                                                          \
+    if (p.tail_splits > 1 || p.sk_tiles > 0)                                                   \
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, true>, a, b, bt, c, p);            \
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, false>, a, b, bt, c, p);             \
   }                                                                                            \
   }
 
@@ -49,12 +57,14 @@
     attr[0].val.clusterDim.x = 2;                                                               \
     attr[0].val.clusterDim.y = 1;                                                               \
     attr[0].val.clusterDim.z = 1;                                                               \
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;                            \
+    attr[1].val.programmaticStreamSerializationAllowed = 1;                                     \
     cfg.attrs = attr;                                                                           \
-    cfg.numAttrs = 1;                                                                           \
+    cfg.numAttrs = 2;                                                                           \
   }                                                                                             \
   cudaError_t gemm_max_clusters_pair##BN(size_t smem, int* clusters) {                          \
     cudaLaunchConfig_t cfg;                                                                     \
-    cudaLaunchAttribute attr[1];                                                                \
+    cudaLaunchAttribute attr[2];                                                                \
     pair_config_##BN(cfg, attr, 2, smem, nullptr);                                              \
     return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false>, &cfg);        \
   }                                                                                             \
@@ -62,7 +72,7 @@
                                    const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid,             \
                                    size_t smem, cudaStream_t stream) {                          \
     cudaLaunchConfig_t cfg;                                                                     \
-    cudaLaunchAttribute attr[1];                                                                \
+    cudaLaunchAttribute attr[2];                                                                \
     pair_config_##BN(cfg, attr, grid, smem, stream);                                            \
     if (p.tail_splits > 1 || p.sk_tiles > 0)                                                                      \
       return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, true>, a, b, bt, c, p);                 \

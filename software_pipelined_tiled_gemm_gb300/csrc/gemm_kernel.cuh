@@ -281,6 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // Programmatic dependent launch: the set-up above touched no global memory
+  // and may overlap the previous kernel's tail; everything below (operand
+  // loads, C stores, workspace and status words) waits for it to finish.
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait_prior_grid();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --

@@ -116,6 +116,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) start its prologue on SMs this grid frees.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding kernel in the stream has completed and its memory
+// operations are visible (a no-op when there is none to wait for).
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
