@@ -128,6 +128,8 @@ struct gemm_plan {
   const void* mapC_ptr = nullptr;
   int64_t mapK = -1;
   CUtensorMap tmA{}, tmB{}, tmBt{}, tmC{};   // tmBt: B box of a narrow tail tile
+  CUtensorMap tmBp{};                        // B, unswizzled 4-slice box, for L2 prefetch
+  int prefetch_kb = 0;
 
   // device staging for gemm_run_host
   void* hA = nullptr;
@@ -143,7 +145,8 @@ namespace {
 
 gemm_status_t encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* base, int64_t inner,
                         int64_t rows, int64_t pitch_elems, uint32_t box_inner, uint32_t box_rows,
-                        CUtensorMapL2promotion l2) {
+                        CUtensorMapL2promotion l2,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
@@ -153,8 +156,7 @@ gemm_status_t encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* base, int
   const CUtensorMapDataType t =
       dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, l2,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for %lld x %lld",
                 static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(inner));
@@ -189,15 +191,15 @@ cudaError_t set_smem(int bn, int cg, size_t smem) {
 }
 
 cudaError_t launch(int bn, int cg, const CUtensorMap& a, const CUtensorMap& b,
-                   const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid,
-                   size_t smem, cudaStream_t s) {
+                   const CUtensorMap& bt, const CUtensorMap& c, const CUtensorMap& bp,
+                   const Params& p, int grid, size_t smem, cudaStream_t s) {
   if (cg == 2)
-    return bn == 128 ? gemm_launch_pair128(a, b, bt, c, p, grid, smem, s)
-                     : gemm_launch_pair256(a, b, bt, c, p, grid, smem, s);
+    return bn == 128 ? gemm_launch_pair128(a, b, bt, c, bp, p, grid, smem, s)
+                     : gemm_launch_pair256(a, b, bt, c, bp, p, grid, smem, s);
   switch (bn) {
-    case 64: return gemm_launch_bn64(a, b, bt, c, p, grid, smem, s);
-    case 128: return gemm_launch_bn128(a, b, bt, c, p, grid, smem, s);
-    default: return gemm_launch_bn256(a, b, bt, c, p, grid, smem, s);
+    case 64: return gemm_launch_bn64(a, b, bt, c, bp, p, grid, smem, s);
+    case 128: return gemm_launch_bn128(a, b, bt, c, bp, p, grid, smem, s);
+    default: return gemm_launch_bn256(a, b, bt, c, bp, p, grid, smem, s);
   }
 }
 
@@ -325,6 +327,14 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     chosen_bufs = bufs;
     chosen_clusters = clusters;
     if (want_bn != 0 || cg == 2 || tiles >= prop.multiProcessorCount) break;
+    // Few tiles: a width whose tiles can be split in two along K (see below)
+    // and then keep at least 80 % of the SMs busy is wide enough.
+    if (cg == 1 && variant == GEMM_PIPELINED && want_split != -1 &&
+        2 * tiles <= prop.multiProcessorCount && 10 * 2 * tiles >= 8 * prop.multiProcessorCount &&
+        cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
+        static_cast<int64_t>(stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
+            static_cast<int64_t>(kEpiWarps) * 32 * bn * 4)
+      break;
   }
   if (chosen == 0) {
     return fail(GEMM_ERR_SMEM_BUDGET,
@@ -385,7 +395,18 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->dp_tiles = p->num_tiles;
   p->tail_splits = 1;
   p->sk_tiles = 0;
-  if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
+  const int64_t ring_all = static_cast<int64_t>(stages) *
+                           (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
+  const bool ring_holds_partial = ring_all >= static_cast<int64_t>(kEpiWarps) * 32 * p->bn * 4;
+  if (variant == GEMM_PIPELINED && want_split == 0 && chosen_cg == 1 && p->num_tiles > 0 &&
+      2 * p->num_tiles <= walkers && k_blocks >= 16 && k_blocks % 2 == 0 && ring_holds_partial) {
+    // Few tiles (at most half a wave): split every tile in two equal K halves
+    // on two walkers -- the stream-K machinery with sk_tiles = tiles and
+    // exactly two walkers per tile (first half owns, second contributes).
+    p->dp_tiles = 0;
+    p->sk_tiles = p->num_tiles;
+    walkers = static_cast<int>(2 * p->num_tiles);
+  } else if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
     const int64_t rem = p->num_tiles % walkers;
     const int64_t ring = static_cast<int64_t>(stages) *
                          (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
@@ -416,6 +437,9 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
       }
     }
   }
+  // One row of tiles streaming a large B (memory-bound): prefetch B into L2
+  // in 512-byte row runs, 8 slices ahead.
+  p->prefetch_kb = (p->tiles_m == 1 && k_blocks >= 4 * kPrefetchSlices) ? 8 : 0;
   const int64_t tail = p->num_tiles - p->dp_tiles;
   p->num_units = p->sk_tiles > 0 ? p->dp_tiles : p->dp_tiles + tail * p->tail_splits;
   if (p->num_units > kMaxDim) {
@@ -546,8 +570,10 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
 
   const bool tma_store = (N % 8) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
 
+  // M <= 64 (single CTA tiles): copy only 64 rows of A per slice.
+  const uint32_t a_box_rows = (plan->cg == 1 && M <= 64) ? 64u : static_cast<uint32_t>(kBM);
   if (plan->mapA_ptr != effA || plan->mapK != Keff) {
-    st = encode_2d(&plan->tmA, plan->dtype, effA, Keff, M, Keff, kBK, kBM,
+    st = encode_2d(&plan->tmA, plan->dtype, effA, Keff, M, Keff, kBK, a_box_rows,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (st != GEMM_OK) return st;
     plan->mapA_ptr = effA;
@@ -563,6 +589,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
       if (st != GEMM_OK) return st;
     } else {
       plan->tmBt = plan->tmB;
+    }
+    if (plan->prefetch_kb > 0) {
+      st = encode_2d(&plan->tmBp, plan->dtype, effB, Keff, N, Keff, kBK * kPrefetchSlices,
+                     static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != GEMM_OK) return st;
+    } else {
+      plan->tmBp = plan->tmB;
     }
     plan->mapB_ptr = effB;
   }
@@ -608,12 +642,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   // so stagger where each starts along K.
   prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
   prm.inject_fault = plan->debug_fault;
+  prm.prefetch_kb = plan->prefetch_kb;
+  prm.a_box_rows = static_cast<int>(a_box_rows);
   prm.sk_tiles = static_cast<int>(plan->sk_tiles);
   prm.sk_ws = plan->sk_ws;
   prm.sk_flags = plan->sk_flags;
 
-  cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC, prm,
-                         plan->grid, plan->smem, stream);
+  cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC,
+                         plan->tmBp, prm, plan->grid, plan->smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
   ++kernels;
   plan->last_pads = (padA || padB) ? 1 : 0;

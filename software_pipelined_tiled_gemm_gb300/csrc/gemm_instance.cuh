@@ -17,8 +17,8 @@
                                 static_cast<int>(smem));                                       \
   }                                                                                            \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,                   \
-                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, \
-                                 int grid, size_t smem, cudaStream_t stream) {                 \
+                                 const CUtensorMap& bt, const CUtensorMap& c, const CUtensorMap& bp, \
+                                 const Params& p, int grid, size_t smem, cudaStream_t stream) {                 \
     cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};                                             \
     cudaLaunchAttribute attr[1];                                                               \
     cfg.gridDim = dim3(grid, 1, 1);                                                            \
@@ -30,8 +30,8 @@
     cfg.attrs = attr;                                                                          \
     cfg.numAttrs = 1;                                                                          \
     if (p.tail_splits > 1 || p.sk_tiles > 0)                                                   \
-      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, true>, a, b, bt, c, p);            \
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, false>, a, b, bt, c, p);             \
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, true>, a, b, bt, c, bp, p);            \
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 1, false>, a, b, bt, c, bp, p);             \
   }                                                                                            \
   }
 
@@ -69,13 +69,13 @@
     return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false>, &cfg);        \
   }                                                                                             \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,                  \
-                                   const CUtensorMap& bt, const CUtensorMap& c, const Params& p, int grid,             \
-                                   size_t smem, cudaStream_t stream) {                          \
+                                   const CUtensorMap& bt, const CUtensorMap& c, const CUtensorMap& bp, \
+                                   const Params& p, int grid, size_t smem, cudaStream_t stream) {                          \
     cudaLaunchConfig_t cfg;                                                                     \
     cudaLaunchAttribute attr[2];                                                                \
     pair_config_##BN(cfg, attr, grid, smem, stream);                                            \
     if (p.tail_splits > 1 || p.sk_tiles > 0)                                                                      \
-      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, true>, a, b, bt, c, p);                 \
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, false>, a, b, bt, c, p);                  \
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, true>, a, b, bt, c, bp, p);                 \
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, 2, false>, a, b, bt, c, bp, p);                  \
   }                                                                                             \
   }

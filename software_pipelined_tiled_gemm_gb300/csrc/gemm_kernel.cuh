@@ -212,7 +212,7 @@ template <int BN, int CG, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
-                   const Params p) {
+                   const __grid_constant__ CUtensorMap tmBp, const Params p) {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
   constexpr int kBRows = BN / CG;                    // B rows this CTA loads
   constexpr uint32_t kStageB = kBRows * kBK * 2;
@@ -305,13 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = nb * BN + (narrow ? x.sub * n_width : 0) + static_cast<int>(rank) * b_rows;
         const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
-        const uint32_t bytes = (kStageA + static_cast<uint32_t>(b_rows) * kBK * 2u) * CG;
+        const uint32_t bytes =
+            (static_cast<uint32_t>(p.a_box_rows) * kBK * 2u + static_cast<uint32_t>(b_rows) * kBK * 2u) *
+            CG;
         const int nk = x.k1 - x.k0;
         const int kr = k_start(x, walker, walkers, p);
         for (int i = 0, kb = x.k0 + kr; i < nk; ++i, kb = (kb + 1 == x.k1) ? x.k0 : kb + 1) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
             ok = false;
             break;
+          }
+          if (p.prefetch_kb > 0 && ((kb - x.k0) & (kPrefetchSlices - 1)) == 0) {
+            // L2 prefetch of this unit's B rows, prefetch_kb slices ahead (wrapping
+            // with the rotated K loop), 4 slices per request.
+            int pk = kb + p.prefetch_kb;
+            if (pk >= x.k1) pk -= (x.k1 - x.k0);
+            if (pk >= x.k0 && pk < x.k1) ptx::tma_prefetch_l2_2d(&tmBp, pk * kBK, b_row);
           }
           const uint32_t sa = sbase + stage * kStage;
           // Test hook: the first slice of CTA 0 is announced but never copied.

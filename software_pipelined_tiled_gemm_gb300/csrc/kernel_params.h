@@ -21,7 +21,8 @@ constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
 
-constexpr int kMaxTailSplits = 4;    // narrow tiles a tail tile may be cut into (N >= 64 each)
+constexpr int kMaxTailSplits = 4;
+constexpr int kPrefetchSlices = 4;   // K slices per L2 prefetch box (4 x 128 B per row)    // narrow tiles a tail tile may be cut into (N >= 64 each)
 
 // Where a device-side wait ran out (status word [1]): role << 16 | wait id.
 constexpr int kDetailProducerEmpty = (1 << 16) | 1;
@@ -74,6 +75,14 @@ struct Params {
   // so CTAs that share the same A rows do not all read the same A slice at
   // the same time (used when a single row of tiles spans the whole grid).
   int k_rotate;
+  // > 0: the producer also prefetches B into L2, prefetch_kb slices ahead,
+  // through a tensor map whose box spans 4 K slices (512 contiguous bytes of
+  // each row): memory-bound shapes then read B in longer runs.
+  int prefetch_kb;
+  // Rows of the A box the copy engine writes per CTA (128, or 64 when M <= 64:
+  // the other 64 rows of the slot are left as they are -- they only feed
+  // output rows >= M, which are never stored).
+  int a_box_rows;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
   // copies of its first K slice (see gemm_tuning_t::debug_fault).
   int inject_fault;

@@ -14,9 +14,9 @@ namespace spgemm {
 #define SPGEMM_DECLARE_BN(BN)                                                              \
   cudaError_t gemm_set_smem_bn##BN(size_t smem);                                           \
   cudaError_t gemm_launch_bn##BN(const CUtensorMap& a, const CUtensorMap& b,               \
-                                 const CUtensorMap& bt, const CUtensorMap& c, const Params& p, \
-                                 int grid, size_t smem,                                    \
-                                 cudaStream_t stream);
+                                 const CUtensorMap& bt, const CUtensorMap& c,              \
+                                 const CUtensorMap& bp, const Params& p, int grid,         \
+                                 size_t smem, cudaStream_t stream);
 SPGEMM_DECLARE_BN(64)
 SPGEMM_DECLARE_BN(128)
 SPGEMM_DECLARE_BN(256)
@@ -28,7 +28,7 @@ SPGEMM_DECLARE_BN(256)
   cudaError_t gemm_max_clusters_pair##BN(size_t smem, int* clusters);                      \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,             \
                                    const CUtensorMap& bt, const CUtensorMap& c,            \
-                                   const Params& p, int grid,                              \
+                                   const CUtensorMap& bp, const Params& p, int grid,       \
                                    size_t smem, cudaStream_t stream);
 SPGEMM_DECLARE_PAIR(128)
 SPGEMM_DECLARE_PAIR(256)

@@ -225,12 +225,13 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.tail_splits = 1;
   p.num_units = p.num_tiles;
   p.idesc_tail = p.idesc;
+  p.a_box_rows = kBM;
   const int grid = static_cast<int>(std::min<int64_t>(tiles, s.sm_count));
   cudaError_t e;
   switch (bn) {
-    case 64: e = gemm_launch_bn64(tmA, tmB, tmB, tmC, p, grid, smem, stream); break;
-    case 128: e = gemm_launch_bn128(tmA, tmB, tmB, tmC, p, grid, smem, stream); break;
-    default: e = gemm_launch_bn256(tmA, tmB, tmB, tmC, p, grid, smem, stream); break;
+    case 64: e = gemm_launch_bn64(tmA, tmB, tmB, tmC, tmB, p, grid, smem, stream); break;
+    case 128: e = gemm_launch_bn128(tmA, tmB, tmB, tmC, tmB, p, grid, smem, stream); break;
+    default: e = gemm_launch_bn256(tmA, tmB, tmB, tmC, tmB, p, grid, smem, stream); break;
   }
   return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -74,6 +74,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Prefetch the 2-D box at (x, y) into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 2-D tiled store of a shared-memory box to (x, y); rows/columns outside the
 // tensor are clipped by the copy engine.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x,

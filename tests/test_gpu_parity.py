@@ -494,3 +494,25 @@ def test_hundred_runs_bit_identical():
     assert all(torch.equal(first, outs[i].view(torch.int16)) for i in range(1, 100))
     st, _, _ = gu.check_full(A, B, "f16", outs[0].cpu())
     assert st["ok"], st
+
+
+@pytest.mark.parametrize("shape", [(64, 4096, 2048), (40, 2048, 1024), (128, 2048, 4096),
+                                   (200, 1024, 2048), (64, 8192, 1100)])
+def test_few_tiles_split_k_in_two_bit_exact(shape):
+    # At most half a wave of tiles: each tile runs as two K halves on two
+    # CTAs (the first half adds the second's partial); M <= 64 also copies
+    # only 64 rows of A per slice.  Two runs of the same plan.
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M, N, K = shape
+    A, B = _int_inputs(M, N, K, "f16", seed=M * 3 + N + K)
+    plan = sg.Plan(M, N, K, "f16", stages=6)
+    info = plan.info()
+    assert info["stream_k"] == 1 and info["grid"] == 2 * info["num_tiles"], info
+    a, b = A.cuda(), B.cuda()
+    for _ in range(2):
+        c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+        assert plan.check()[0] == 0
+        _assert_bit_exact(A, B, "f16", c.cpu())
+    plan.close()
