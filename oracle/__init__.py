@@ -11,6 +11,7 @@ over output rows).  This wrapper only marshals numpy arrays through ctypes.
 Definitions followed (see the C file for the full statement):
   * TileLang tutorial ch. 11, "pipelined_gemm.py", matmul_auto: A (M,K),
     B (N,K), C (M,N), ``T.gemm(..., transpose_B=True)``, fp32 accumulator.
+  * ReLU, max(x, 0), the clamp of the Triton lecture notes' matmul example.
   * tanh-GELU as written in the Triton lecture notes ("GeLU") and the
     XLA:GPU emitters page (loop-emitter example, ``@gelu``), constant
     sqrt(2/pi) = 0.7978845608.
@@ -110,6 +111,13 @@ class use_library:
         return False
 
 
+_EPI = {None: 0, "none": 0, 0: 0, "gelu": 1, "gelu_tanh": 1, 1: 1, "relu": 2, 2: 2}
+
+
+def _epi(epilogue) -> int:
+    return _EPI[epilogue]
+
+
 def _dt(dtype) -> int:
     if isinstance(dtype, int):
         return dtype
@@ -151,8 +159,7 @@ def gemm_nt(A, B, dtype, epilogue=None, threads: int = 0) -> np.ndarray:
     N = b.shape[0]
     C = np.zeros((M, N), dtype=np.float64)
     rc = lib.oracle_gemm_nt(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), M, N, K,
-                            _dt(dtype), 1 if epilogue in ("gelu", "gelu_tanh", 1) else 0,
-                            _ptr(C, ctypes.c_double), int(threads))
+                            _dt(dtype), _epi(epilogue), _ptr(C, ctypes.c_double), int(threads))
     if rc != 0:
         raise RuntimeError("oracle_gemm_nt failed")
     return C
@@ -170,7 +177,7 @@ def gemm_nt_entries(A, B, dtype, rows, cols, epilogue=None, threads: int = 0) ->
         raise ValueError("rows and cols must have the same shape")
     out = np.zeros(r.shape, dtype=np.float64)
     rc = lib.oracle_gemm_nt_entries(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), M, N, K,
-                                    _dt(dtype), 1 if epilogue in ("gelu", "gelu_tanh", 1) else 0,
+                                    _dt(dtype), _epi(epilogue),
                                     _ptr(r, ctypes.c_int64), _ptr(c, ctypes.c_int64), r.size,
                                     _ptr(out, ctypes.c_double), int(threads))
     if rc != 0:

@@ -15,6 +15,9 @@
  *    definition C[i,j] = sum_k A[i,k] * B[j,k] and accumulates in fp64, which
  *    is exact for every product of two fp16/bf16 values and leaves only a
  *    ~1e-12 relative sum error at K <= 8192.
+ *  - ReLU epilogue: max(x, 0), the accumulator clamp of the Triton lecture
+ *    notes' matmul example (matmul_relu_kernel); zero and negative sums give
+ *    +0.
  *  - Epilogue: the tanh-approximate GELU, 0.5 x (1 + tanh(sqrt(2/pi) (x +
  *    0.044715 x^3))), as the Triton lecture notes ("GeLU" example) and the
  *    XLA:GPU emitters page (loop-emitter example, function @gelu) write it;
@@ -113,10 +116,20 @@ static uint16_t round_generic(double x, int mant_bits, int emin, int exp_bits) {
 uint16_t oracle_double_to_f16(double x) { return round_generic(x, 10, -14, 5); }
 uint16_t oracle_double_to_bf16(double x) { return round_generic(x, 7, -126, 8); }
 
+/* ---- ReLU ---- */
+double oracle_relu(double x) { return x > 0.0 ? x : 0.0; }
+
 /* ---- tanh-GELU ---- */
 double oracle_gelu_tanh(double x) {
   const double c = 0.7978845608; /* sqrt(2/pi) */
   return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+/* Epilogue selector: 0 none, 1 tanh-GELU, 2 ReLU. */
+static double apply_epilogue(double s, int epilogue) {
+  if (epilogue == 1) return oracle_gelu_tanh(s);
+  if (epilogue == 2) return oracle_relu(s);
+  return s;
 }
 
 static void set_threads(int threads) {
@@ -144,7 +157,8 @@ static double* decode_matrix(const uint16_t* bits, int64_t count, int dtype) {
   return out;
 }
 
-/* C[i,j] = sum_k A[i,k] * B[j,k] (+ GELU when epilogue == 1), all in fp64.
+/* C[i,j] = epi(sum_k A[i,k] * B[j,k]), all in fp64; epilogue 0 none,
+ * 1 tanh-GELU, 2 ReLU.
  * A: M x K row-major, B: N x K row-major, C: M x N row-major doubles.
  * Returns 0 on success, -1 on bad arguments or allocation failure. */
 int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
@@ -162,7 +176,7 @@ int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, i
       const double* b = Bd + j * K;
       double s = 0.0;
       for (int64_t k = 0; k < K; ++k) s += a[k] * b[k];
-      C[i * N + j] = epilogue == 1 ? oracle_gelu_tanh(s) : s;
+      C[i * N + j] = apply_epilogue(s, epilogue);
     }
   }
   free(Ad);
@@ -185,7 +199,7 @@ int oracle_gemm_nt_entries(const uint16_t* A, const uint16_t* B, int64_t M, int6
     const uint16_t* b = B + cols[t] * K;
     double s = 0.0;
     for (int64_t k = 0; k < K; ++k) s += oracle_decode(a[k], dtype) * oracle_decode(b[k], dtype);
-    out[t] = epilogue == 1 ? oracle_gelu_tanh(s) : s;
+    out[t] = apply_epilogue(s, epilogue);
   }
   return 0;
 }

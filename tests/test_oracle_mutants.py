@@ -32,8 +32,10 @@ MUTANTS = {
     "round_ties_away": ("nearbyint(ldexp(a, -q))", "round(ldexp(a, -q))"),
     "entries_wrong_row": ("const uint16_t* a = A + rows[t] * K;",
                           "const uint16_t* a = A + cols[t] * K;"),
-    "gelu_skipped_in_gemm": ("C[i * N + j] = epilogue == 1 ? oracle_gelu_tanh(s) : s;",
-                             "C[i * N + j] = s;"),
+    "gelu_skipped_in_gemm": ("if (epilogue == 1) return oracle_gelu_tanh(s);",
+                             "if (epilogue == 9) return oracle_gelu_tanh(s);"),
+    "relu_reflects": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : -x;"),
+    "relu_leaky": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : 0.01 * x;"),
 }
 
 PIN_TESTS = [
@@ -54,6 +56,8 @@ PIN_TESTS = [
     lambda: pins.test_gelu_zero_and_odd_even_identity(),
     lambda: pins.test_gelu_close_to_erf_gelu_with_known_max_error(),
     lambda: pins.test_gemm_gelu_epilogue_applies_after_sum(),
+    lambda: pins.test_relu_epilogue_on_a_transposed_identity(),
+    lambda: pins.test_relu_epilogue_is_the_triton_clamp(),
 ]
 
 

@@ -324,3 +324,29 @@ def test_bf16_rounding_floor_exceeds_frobenius_bound():
     bad = rnd.copy()
     bad[5, 7] += 3 * tolerance.ulp(ref[5, 7], "bf16") + 1.001e-3
     assert not tolerance.compare(bad, ref, "bf16")["ok"]
+
+
+# -------------------------------------------------------------- ReLU pins --
+
+def test_relu_epilogue_on_a_transposed_identity():
+    # A = I makes C = B^T exactly; with the ReLU epilogue every negative entry
+    # of B^T must become +0 and every positive one stay as it is.
+    K, N = 24, 13
+    _, B = gemm_inputs.custom(1, N, K, dist="int", lo=-3, hi=3, seed=17)
+    I = oracle.round_to(np.eye(K), "f16")
+    C = oracle.gemm_nt(I, B, "f16", epilogue="relu")
+    bt = B.to(torch.float64).numpy().T
+    want = np.where(bt > 0, bt, 0.0)
+    assert np.array_equal(C, want)
+    assert not np.any(np.signbit(C))           # no -0
+
+
+def test_relu_epilogue_is_the_triton_clamp():
+    # matmul_relu_kernel: acc = max(acc, 0) on the fp32 accumulator; in exact
+    # arithmetic that is the positive part of the plain product, which the
+    # integer case pins independently of the oracle (numpy int64 matmul).
+    A, B = gemm_inputs.custom(40, 30, 64, dist="int", lo=-2, hi=2, seed=18)
+    C = oracle.gemm_nt(A, B, "f16", epilogue="relu")
+    exact = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T
+    assert np.array_equal(C, np.maximum(exact, 0).astype(np.float64))
+    assert (exact < 0).any() and (exact > 0).any()
