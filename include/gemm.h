@@ -30,7 +30,8 @@
  * Layout.  All matrices are row-major and dense: A has K elements per row
  * (lda = K), B has K elements per row (ldb = K), C has N elements per row
  * (ldc = N).  Both operands are therefore K-contiguous ("K-major").
- * Element type of A, B and C is `dtype`.  Pointers A, B, C are device
+ * Element type of A and B is `dtype`; C has the same type, or fp32 when the
+ * plan was created with gemm_tuning_t.out_f32 = 1.  Pointers A, B, C are device
  * pointers (cudaMalloc / torch CUDA tensors) on the plan's device, except for
  * gemm_run_host, which takes host pointers.
  *
@@ -78,7 +79,9 @@ typedef enum {
 
 typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
 
-typedef enum { GEMM_EPI_NONE = 0, GEMM_EPI_GELU_TANH = 1 } gemm_epilogue_t;
+/* Epilogue applied to the fp32 accumulator before the output rounding:
+ * GEMM_EPI_RELU is max(x, 0) (the Triton lecture notes' matmul example). */
+typedef enum { GEMM_EPI_NONE = 0, GEMM_EPI_GELU_TANH = 1, GEMM_EPI_RELU = 2 } gemm_epilogue_t;
 
 typedef enum {
   GEMM_PIPELINED = 0,     /* `stages`-deep ring, double-buffered accumulator */
@@ -102,6 +105,9 @@ typedef struct {
                           k in {2, 3, 4} = cut each leftover tile along N into k
                           narrower tiles (>= 64 columns each, k must divide tile_n) */
   int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
+  int out_f32;         /* 1: C is fp32 (4-byte elements, written unrounded from the fp32
+                          accumulator after the epilogue), as in the Triton lecture notes'
+                          matmul example; 0: C has the inputs' 16-bit type */
   int debug_fault;     /* test hook, 0 in normal use.  1: the first CTA's copy engine
                           never receives its first K slice, so the pipeline's waits run
                           out their time limit and gemm_plan_check reports
@@ -126,6 +132,7 @@ typedef struct {
   int tail_splits;             /* narrow tiles per cut tile (1 = none) */
   int64_t work_units;          /* whole tiles + narrow tiles walked by the CTAs */
   int stream_k;                /* 1: the tail_tiles are shared out stream-K */
+  int out_f32;                 /* C is fp32 */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

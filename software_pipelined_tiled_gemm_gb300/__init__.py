@@ -30,7 +30,7 @@ __all__ = [
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
     "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
-    "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH",
+    "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH", "GEMM_EPI_RELU",
     "GEMM_PIPELINED", "GEMM_SINGLE_BUFFER",
 ]
 
@@ -49,6 +49,7 @@ GEMM_F16 = 0
 GEMM_BF16 = 1
 GEMM_EPI_NONE = 0
 GEMM_EPI_GELU_TANH = 1
+GEMM_EPI_RELU = 2
 GEMM_PIPELINED = 0
 GEMM_SINGLE_BUFFER = 1
 
@@ -57,7 +58,7 @@ class GemmTuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
-                ("debug_fault", ctypes.c_int)]
+                ("out_f32", ctypes.c_int), ("debug_fault", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -69,7 +70,7 @@ class GemmPlanInfo(ctypes.Structure):
                 ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("cta_group", ctypes.c_int), ("tail_tiles", ctypes.c_int64),
                 ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64),
-                ("stream_k", ctypes.c_int)]
+                ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -217,7 +218,7 @@ def gemm_plan_destroy(plan):
 
 _DT = {"f16": GEMM_F16, "bf16": GEMM_BF16}
 _EPI = {None: GEMM_EPI_NONE, "none": GEMM_EPI_NONE, "gelu": GEMM_EPI_GELU_TANH,
-        "gelu_tanh": GEMM_EPI_GELU_TANH}
+        "gelu_tanh": GEMM_EPI_GELU_TANH, "relu": GEMM_EPI_RELU}
 _VAR = {"pipelined": GEMM_PIPELINED, "single_buffer": GEMM_SINGLE_BUFFER}
 
 
@@ -235,7 +236,7 @@ class Plan:
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
                  tile_n=0, raster_group=0, max_ctas=0, cta_group=0, tail_split=0,
-                 timeout_ns=0, debug_fault=0):
+                 timeout_ns=0, out_f32=0, debug_fault=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -244,7 +245,7 @@ class Plan:
         self.device = int(device)
         self._h = None
         tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
-                            int(tail_split), int(timeout_ns), int(debug_fault))
+                            int(tail_split), int(timeout_ns), int(out_f32), int(debug_fault))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")
@@ -306,12 +307,14 @@ def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", devic
         return p
 
 
-def matmul_nt(A, B, epilogue=None, stages: int = 4, variant: str = "pipelined", out=None,
-              **tuning):
+def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", out=None,
+              out_dtype=None, **tuning):
     """C = epi(A @ B.T) on the current CUDA stream.
 
     A: (M, K) and B: (N, K) CUDA tensors of the same dtype (float16 or
-    bfloat16), contiguous.  Returns C (M, N) of that dtype (``out`` if given).
+    bfloat16), contiguous.  epilogue: None, "gelu" or "relu".  Returns C
+    (M, N) of that dtype, or of float32 when out_dtype is torch.float32
+    (``out`` if given).
     """
     import torch
     if not (A.is_cuda and B.is_cuda):
@@ -327,11 +330,16 @@ def matmul_nt(A, B, epilogue=None, stages: int = 4, variant: str = "pipelined", 
     dt = _torch_dtype_code(A)
     M, K = A.shape
     N = B.shape[0]
+    c_dtype = out_dtype if out_dtype is not None else (out.dtype if out is not None else A.dtype)
+    if c_dtype not in (A.dtype, torch.float32):
+        raise TypeError("C must have A's dtype or float32")
     if out is None:
-        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    elif out.shape != (M, N) or out.dtype != A.dtype or not out.is_contiguous() or out.device != A.device:
-        raise ValueError("out must be a contiguous (M, N) tensor of A's dtype on A's device")
+        out = torch.empty((M, N), dtype=c_dtype, device=A.device)
+    elif out.shape != (M, N) or out.dtype != c_dtype or not out.is_contiguous() or out.device != A.device:
+        raise ValueError("out must be a contiguous (M, N) tensor of the output dtype on A's device")
     dtype = "bf16" if dt == GEMM_BF16 else "f16"
+    if c_dtype == torch.float32:
+        tuning["out_f32"] = 1
     plan = get_plan(M, N, K, dtype, epilogue, stages, variant, A.device.index or 0, **tuning)
     plan.run(A, B, out)
     return out

@@ -111,6 +111,7 @@ struct gemm_plan {
   size_t smem = 0;
   unsigned long long timeout_ns = kDefaultTimeoutNs;
   int debug_fault = 0;
+  int out_f32 = 0;               // C element: 0 = input type, 1 = fp32
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -163,6 +164,24 @@ gemm_status_t encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* base, int
   return GEMM_OK;
 }
 
+// fp32 C: 2-D map with 4-byte elements, 128-byte swizzle (box rows of 128 B).
+gemm_status_t encode_2d_f32(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                            int64_t pitch_elems, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 4u};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 C) failed (CUresult %d)",
+                static_cast<int>(r));
+  return GEMM_OK;
+}
+
 gemm_status_t check_common(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                            gemm_epilogue_t epi, int stages) {
   if (M < 0 || N < 0 || K < 0)
@@ -172,7 +191,7 @@ gemm_status_t check_common(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
     return fail(GEMM_ERR_INVALID_ARG, "size above 2^31-1");
   if (dtype != GEMM_F16 && dtype != GEMM_BF16)
     return fail(GEMM_ERR_INVALID_ARG, "dtype %d out of range", static_cast<int>(dtype));
-  if (epi != GEMM_EPI_NONE && epi != GEMM_EPI_GELU_TANH)
+  if (epi != GEMM_EPI_NONE && epi != GEMM_EPI_GELU_TANH && epi != GEMM_EPI_RELU)
     return fail(GEMM_ERR_INVALID_ARG, "epilogue %d out of range", static_cast<int>(epi));
   if (stages < 1 || stages > kMaxStages)
     return fail(GEMM_ERR_INVALID_ARG, "stages %d outside [1, %d]", stages, kMaxStages);
@@ -267,6 +286,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
     if (tuning->debug_fault < 0 || tuning->debug_fault > 1)
       return fail(GEMM_ERR_INVALID_ARG, "debug_fault %d not in {0, 1}", tuning->debug_fault);
+    if (tuning->out_f32 < 0 || tuning->out_f32 > 1)
+      return fail(GEMM_ERR_INVALID_ARG, "out_f32 %d not in {0, 1}", tuning->out_f32);
     if (tuning->timeout_ns > 0) timeout = static_cast<unsigned long long>(tuning->timeout_ns);
   }
 
@@ -358,6 +379,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->num_acc = variant == GEMM_SINGLE_BUFFER ? 1 : 2;
   p->max_ctas = want_ctas;
   p->debug_fault = tuning ? tuning->debug_fault : 0;
+  p->out_f32 = tuning ? tuning->out_f32 : 0;
   p->bn = chosen;
   p->cg = chosen_cg;
   p->smem = chosen_smem;
@@ -510,13 +532,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   }
   if (!C) return fail(GEMM_ERR_INVALID_ARG, "C is NULL");
   if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+  const size_t esC = plan->out_f32 ? 4 : 2;   // bytes per element of C
   const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
-  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  const size_t bytesC = static_cast<size_t>(M) * N * esC;
   if (ranges_overlap(C, bytesC, A, bytesA) || ranges_overlap(C, bytesC, B, bytesB))
     return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
-  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
-       reinterpret_cast<uintptr_t>(C)) & 1u)
-    return fail(GEMM_ERR_INVALID_ARG, "A, B and C must be 2-byte aligned");
+  if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u) ||
+      (reinterpret_cast<uintptr_t>(C) & (esC - 1)) != 0)
+    return fail(GEMM_ERR_INVALID_ARG, "A and B must be 2-byte and C %zu-byte aligned", esC);
 
   DeviceGuard guard(plan->device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
@@ -568,7 +591,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const int64_t Keff = (padA || padB) ? Kp : K;
   // If only one operand is padded, the other's pitch is K == Kp (K % 8 == 0).
 
-  const bool tma_store = (N % 8) == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+  const bool tma_store =
+      (static_cast<size_t>(N) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
 
   // M <= 64 (single CTA tiles): copy only 64 rows of A per slice.
   const uint32_t a_box_rows = (plan->cg == 1 && M <= 64) ? 64u : static_cast<uint32_t>(kBM);
@@ -602,8 +626,10 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   }
   plan->mapK = Keff;
   if (tma_store && plan->mapC_ptr != C) {
-    st = encode_2d(&plan->tmC, plan->dtype, C, N, M, N, kStoreCols, 32,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    // One 128-byte row of 16-bit (64) or fp32 (32) elements per box row.
+    st = plan->out_f32 ? encode_2d_f32(&plan->tmC, C, N, M, N, 32, 32)
+                       : encode_2d(&plan->tmC, plan->dtype, C, N, M, N, kStoreCols, 32,
+                                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (st != GEMM_OK) return st;
     plan->mapC_ptr = C;
   }
@@ -626,7 +652,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.raster_group = plan->raster_group;
   prm.store_bufs = plan->store_bufs;
   prm.bf16 = plan->dtype == GEMM_BF16 ? 1 : 0;
-  prm.gelu = plan->epi == GEMM_EPI_GELU_TANH ? 1 : 0;
+  prm.epilogue = static_cast<int>(plan->epi);
+  prm.out_f32 = plan->out_f32;
   prm.tma_store = tma_store ? 1 : 0;
   prm.idesc = ptx::instr_desc_f16(kBM * plan->cg, plan->bn, plan->dtype == GEMM_BF16);
   prm.C = C;
@@ -669,7 +696,7 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
       stages != plan->stages)
     return fail(GEMM_ERR_PLAN_MISMATCH, "run arguments differ from the plan");
   const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
-  const size_t bytesC = static_cast<size_t>(M) * N * 2;
+  const size_t bytesC = static_cast<size_t>(M) * N * (plan->out_f32 ? 4 : 2);
   if (bytesC == 0) return GEMM_OK;
   if (!hC || (bytesA && !hA) || (bytesB && !hB))
     return fail(GEMM_ERR_INVALID_ARG, "NULL host buffer");
@@ -737,6 +764,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->tail_splits = plan->tail_splits;
   info->work_units = plan->num_units;
   info->stream_k = plan->sk_tiles > 0 ? 1 : 0;
+  info->out_f32 = plan->out_f32;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
   return GEMM_OK;
 }

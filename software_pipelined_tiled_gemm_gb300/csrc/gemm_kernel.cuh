@@ -201,6 +201,81 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Epilogue functions on an fp32 accumulator value: 0 identity, 1 tanh-GELU,
+// 2 ReLU (max(x, 0), with -0 and NaN giving +0).
+__device__ __forceinline__ float apply_epilogue(float x, int epilogue) {
+  if (epilogue == 1) return gelu_tanh(x);
+  if (epilogue == 2) return x > 0.0f ? x : 0.0f;
+  return x;
+}
+
+// Store one 32-row x 128-byte block of C held as 32 words per lane (lane =
+// row, words = the row's 128 bytes): `esize`-byte elements starting at
+// column col0 of rows row0 .. row0+31.  The block goes through the warp's
+// staging buffer in the layout of a 128-byte-swizzled TMA box (16-byte chunk
+// j of row r at j ^ (r % 8): bank-conflict free), then out with one TMA store
+// (double-buffered staging), or -- when C's pitch or address is not 16-byte
+// aligned -- row by row, each store instruction covering one contiguous row
+// segment.
+__device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params& p,
+                                           const CUtensorMap& tmC, uint8_t* my_stage, int& buf,
+                                           int lane, int row0, int col0, int esize) {
+  if (p.tma_store) {
+    // The staging buffer about to be written must have been read out by the
+    // store issued store_bufs blocks ago.
+    if (lane == 0) {
+      if (p.store_bufs == 2)
+        ptx::bulk_wait_group_read<1>();
+      else
+        ptx::bulk_wait_group_read<0>();
+    }
+    __syncwarp();
+    uint8_t* sb = my_stage + buf * kStoreBuf;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+      *reinterpret_cast<uint4*>(sb + off) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(&tmC, ptx::smem_addr(sb), col0, row0);
+      ptx::bulk_commit_group();
+    }
+    buf = (buf + 1 == p.store_bufs) ? 0 : buf + 1;
+  } else {
+    __syncwarp();  // the previous block's reads of the buffer are done
+    uint8_t* sb = my_stage;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+      *reinterpret_cast<uint4*>(sb + off) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+    __syncwarp();
+    const int per_row = 128 / esize;                       // elements in the block's row
+    const int ncols = min(per_row, p.N - col0);
+    const int nrows = min(32, p.M - row0);
+#pragma unroll 1
+    for (int r = 0; r < nrows; ++r) {
+      uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) +
+                      (static_cast<int64_t>(row0 + r) * p.ldc + col0) * esize;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int cc = lane + 32 * h;                      // element index in the row
+        if (cc < ncols) {
+          const uint32_t byte = static_cast<uint32_t>(cc * esize);
+          const uint32_t off = static_cast<uint32_t>(r) * 128u +
+                               (((byte >> 4) ^ (static_cast<uint32_t>(r) & 7u)) << 4) + (byte & 15u);
+          if (esize == 2)
+            *reinterpret_cast<uint16_t*>(crow + cc * 2) = *reinterpret_cast<const uint16_t*>(sb + off);
+          else
+            *reinterpret_cast<uint32_t*>(crow + cc * 4) = *reinterpret_cast<const uint32_t*>(sb + off);
+        }
+      }
+    }
+  }
+}
+
 // BN: output tile width.  CG: CTAs per tile (1, or 2 for a CTA pair that
 // computes a 256 x BN tile with cta_group::2 MMAs: each CTA loads its own 128
 // rows of A and BN/2 rows of B, the even CTA issues the MMAs for both, and
@@ -503,78 +578,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               r1[j] = __float_as_uint(__uint_as_float(r1[j]) + fix[(cb + 32 + j) * 32 + lane]);
             }
           }
-          uint32_t pk[32];
+          // Epilogue function on the fp32 accumulator values.
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float a0 = __uint_as_float(r0[2 * j]), a1 = __uint_as_float(r0[2 * j + 1]);
-            float b0 = __uint_as_float(r1[2 * j]), b1 = __uint_as_float(r1[2 * j + 1]);
-            if (p.gelu) {
-              a0 = gelu_tanh(a0);
-              a1 = gelu_tanh(a1);
-              b0 = gelu_tanh(b0);
-              b1 = gelu_tanh(b1);
-            }
-            pk[j] = pack2(a0, a1, bf16);
-            pk[16 + j] = pack2(b0, b1, bf16);
+          for (int j = 0; j < 32; ++j) {
+            r0[j] = __float_as_uint(apply_epilogue(__uint_as_float(r0[j]), p.epilogue));
+            r1[j] = __float_as_uint(apply_epilogue(__uint_as_float(r1[j]), p.epilogue));
           }
-          if (p.tma_store) {
-            // The staging buffer about to be written must have been read out
-            // by the store issued store_bufs chunks ago.
-            if (lane == 0) {
-              if (p.store_bufs == 2)
-                ptx::bulk_wait_group_read<1>();
-              else
-                ptx::bulk_wait_group_read<0>();
-            }
-            __syncwarp();
-            uint8_t* sb = my_stage + buf * kStoreBuf;
-            // Row `lane` is 128 B; 16-byte chunk j lands at j ^ (row % 8),
-            // the layout of a 128-byte-swizzled TMA box.
+          if (!p.out_f32) {
+            // Round to fp16/bf16: 64 columns = 32 packed words = one 128-byte row.
+            uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
-              *reinterpret_cast<uint4*>(sb + off) =
-                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 16; ++j) {
+              pk[j] = pack2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), bf16);
+              pk[16 + j] = pack2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), bf16);
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_2d(&tmC, ptx::smem_addr(sb), col0, row0);
-              ptx::bulk_commit_group();
-            }
-            buf = (buf + 1 == p.store_bufs) ? 0 : buf + 1;
+            store_rows(pk, p, tmC, my_stage, buf, lane, row0, col0, 2);
           } else {
-            // C's pitch or address is not 16-byte aligned, so no TMA store:
-            // stage the 32 x 64 chunk in shared memory (same swizzled layout)
-            // and write it out a row at a time, each store instruction
-            // covering 64 contiguous bytes of one row.
-            __syncwarp();  // the previous chunk's reads of the buffer are done
-            uint8_t* sb = my_stage;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t off = lane * 128u + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
-              *reinterpret_cast<uint4*>(sb + off) =
-                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            }
-            __syncwarp();
-            const int ncols = min(kStoreCols, p.N - col0);
-            const int nrows = min(32, p.M - row0);
-#pragma unroll 1
-            for (int r = 0; r < nrows; ++r) {
-              uint16_t* crow =
-                  reinterpret_cast<uint16_t*>(p.C) + static_cast<int64_t>(row0 + r) * p.ldc + col0;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int cc = lane + 32 * h;
-                if (cc < ncols) {
-                  const uint32_t off =
-                      static_cast<uint32_t>(r) * 128u +
-                      ((static_cast<uint32_t>(cc >> 3) ^ (static_cast<uint32_t>(r) & 7u)) << 4) +
-                      static_cast<uint32_t>(cc & 7) * 2u;
-                  crow[cc] = *reinterpret_cast<const uint16_t*>(sb + off);
-                }
-              }
-            }
+            // fp32 output: each 32-column half is one 128-byte row.
+            store_rows(r0, p, tmC, my_stage, buf, lane, row0, col0, 4);
+            store_rows(r1, p, tmC, my_stage, buf, lane, row0, col0 + 32, 4);
           }
         }
       }

@@ -46,7 +46,8 @@ struct Params {
   int raster_group;      // tile rows per raster group
   int store_bufs;        // staging buffers per epilogue warp (1 or 2)
   int bf16;              // element type: 0 fp16, 1 bf16
-  int gelu;              // epilogue: 0 none, 1 tanh-GELU
+  int epilogue;          // 0 none, 1 tanh-GELU, 2 ReLU
+  int out_f32;           // C element type: 0 = the input type, 1 = fp32
   int tma_store;         // 1: bulk tensor stores of C; 0: masked st.global
   uint32_t idesc;        // tcgen05.mma instruction descriptor
   void* C;               // used by the st.global path

@@ -125,7 +125,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return GEMM_ERR_INVALID_ARG;
   if ((dtype != GEMM_F16 && dtype != GEMM_BF16) ||
-      (epi != GEMM_EPI_NONE && epi != GEMM_EPI_GELU_TANH) || stages < 1 || stages > kMaxStages)
+      (epi != GEMM_EPI_NONE && epi != GEMM_EPI_GELU_TANH && epi != GEMM_EPI_RELU) || stages < 1 ||
+      stages > kMaxStages)
     return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
   if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
@@ -214,7 +215,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.raster_group = static_cast<int>(std::min<int64_t>(16, tm));
   p.store_bufs = bufs;
   p.bf16 = dtype == GEMM_BF16 ? 1 : 0;
-  p.gelu = epi == GEMM_EPI_GELU_TANH ? 1 : 0;
+  p.epilogue = static_cast<int>(epi);
+  p.out_f32 = 0;
   p.tma_store = tma_store ? 1 : 0;
   p.idesc = ptx::instr_desc_f16(kBM, bn, dtype == GEMM_BF16);
   p.C = C;

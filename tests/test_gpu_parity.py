@@ -516,3 +516,75 @@ def test_few_tiles_split_k_in_two_bit_exact(shape):
         assert plan.check()[0] == 0
         _assert_bit_exact(A, B, "f16", c.cpu())
     plan.close()
+
+
+
+# ------------------------------------------- ReLU epilogue, fp32 output --
+
+def _run_f32(A, B, dtype, epilogue=None, c_offset=0, **tuning):
+    """C = epi(A.B^T) with fp32 C through gemm_run; returns (C_cpu, info, canary_ok)."""
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M, K = A.shape
+    N = B.shape[0]
+    cbuf = torch.full((M * N + c_offset + 32,), -7.0, dtype=torch.float32, device="cuda")
+    c = cbuf[c_offset:c_offset + M * N]
+    plan = sg.Plan(M, N, K, dtype, epilogue, out_f32=1, **tuning)
+    a, b = A.cuda(), B.cuda()          # keep the device copies alive during the run
+    plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert plan.check()[0] == 0
+    info = plan.info()
+    plan.close()
+    around = torch.cat([cbuf[:c_offset], cbuf[c_offset + M * N:]])
+    return c.view(M, N).cpu(), info, bool((around == -7.0).all())
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_relu_epilogue_bit_exact(dtype, cta_group):
+    A, B = _int_inputs(384, 640, 256, dtype, seed=51)
+    C, info, canary = gu.run_device(A, B, dtype, epilogue="relu", cta_group=cta_group)
+    want = oracle.round_to(oracle.gemm_nt(A, B, dtype, epilogue="relu"), dtype)
+    assert canary and (gu.bits(C) == want).all()
+
+
+def test_relu_epilogue_general_values_and_unaligned_c():
+    A, B = gemm_inputs.custom(300, 261, 520, dist="normal_scaled", seed=52)
+    for off in (0, 1):
+        C, info, canary = gu.run_device(A, B, "f16", epilogue="relu", c_offset=off)
+        st, _, _ = gu.check_full(A, B, "f16", C, epilogue="relu")
+        assert canary and st["ok"] and (C.float() >= 0).all(), (off, st)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_fp32_output_exact_on_integers(cta_group):
+    A, B = _int_inputs(512, 768, 640, "f16", seed=53)
+    C, info, canary = _run_f32(A, B, "f16", cta_group=cta_group)
+    assert info["out_f32"] == 1 and canary
+    exact = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T
+    assert np.array_equal(C.numpy().astype(np.float64), exact.astype(np.float64))
+
+
+@pytest.mark.parametrize("epilogue", [None, "gelu", "relu"])
+@pytest.mark.parametrize("shape,c_offset", [((256, 512, 512), 0), ((300, 261, 264), 0),
+                                            ((200, 264, 136), 1)])
+def test_fp32_output_within_tolerance(epilogue, shape, c_offset):
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, dtype="bf16", dist="normal_xw", seed=M + N)
+    C, info, canary = _run_f32(A, B, "bf16", epilogue=epilogue, c_offset=c_offset)
+    ref = oracle.gemm_nt(A, B, "bf16", epilogue=epilogue)
+    st = tolerance.compare(C.numpy().astype(np.float64), ref, "f32")
+    assert canary and st["ok"], (shape, epilogue, st, info)
+    assert info["tma_store"] == (1 if (N % 4 == 0 and c_offset % 4 == 0) else 0)
+
+
+def test_fp32_output_stream_k_and_matmul_nt():
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = _int_inputs(768, 1024, 1024, "bf16", seed=54)
+    C, info, canary = _run_f32(A, B, "bf16", cta_group=2, tile_n=256, max_ctas=10, tail_split=1)
+    assert info["stream_k"] == 1 and canary
+    exact = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T
+    assert np.array_equal(C.numpy().astype(np.float64), exact.astype(np.float64))
+    c2 = sg.matmul_nt(A.cuda(), B.cuda(), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert c2.dtype == torch.float32 and torch.equal(c2.cpu(), C)

@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import numpy as np
 
-_FMT = {"f16": (10, -14), "bf16": (7, -126)}
+_FMT = {"f16": (10, -14), "bf16": (7, -126), "f32": (23, -126)}
 
 ULPS = 2.0
 ABS = 1e-3
@@ -53,7 +53,7 @@ def compare(got, ref, dtype: str, ulps: float = ULPS, abs_tol: float = ABS):
     finite = np.isfinite(g)
     bad = (~finite) | (err > bound)
     nr = np.linalg.norm(r)
-    frob_base = r if dtype == "f16" else rounded_reference(r, dtype)
+    frob_base = r if dtype in ("f16", "f32") else rounded_reference(r, dtype)
     diff = np.where(finite, g - frob_base, np.inf)
     frob = float(np.linalg.norm(diff) / nr) if nr > 0 else float(np.linalg.norm(diff))
     frob_exact = float(np.linalg.norm(np.where(finite, g - r, np.inf)) / nr) if nr > 0 else 0.0
