@@ -29,7 +29,9 @@
  *
  * Layout.  All matrices are row-major and dense: A has K elements per row
  * (lda = K), B has K elements per row (ldb = K), C has N elements per row
- * (ldc = N).  Both operands are therefore K-contiguous ("K-major").
+ * (ldc = N).  Both operands are therefore K-contiguous ("K-major").  With
+ * gemm_tuning_t.b_kn = 1, B is instead K x N (ldb = N) and the GEMM is
+ * C = epi(A . B).
  * Element type of A and B is `dtype`; C has the same type, or fp32 when the
  * plan was created with gemm_tuning_t.out_f32 = 1.  Pointers A, B, C are device
  * pointers (cudaMalloc / torch CUDA tensors) on the plan's device, except for
@@ -105,6 +107,10 @@ typedef struct {
                           k in {2, 3, 4} = cut each leftover tile along N into k
                           narrower tiles (>= 64 columns each, k must divide tile_n) */
   int64_t timeout_ns;  /* per-wait limit on the device; 0 = default (2 s), <0 = invalid */
+  int b_kn;            /* 1: B is stored K x N (row-major, N contiguous, ldb = N), so
+                          C = epi(A . B) -- the [M,K] @ [K,N] form of the Mosaic GPU
+                          guide's Hopper example; 0 (default): B is N x K and
+                          C = epi(A . B^T) */
   int out_f32;         /* 1: C is fp32 (4-byte elements, written unrounded from the fp32
                           accumulator after the epilogue), as in the Triton lecture notes'
                           matmul example; 0: C has the inputs' 16-bit type */
@@ -133,6 +139,7 @@ typedef struct {
   int64_t work_units;          /* whole tiles + narrow tiles walked by the CTAs */
   int stream_k;                /* 1: the tail_tiles are shared out stream-K */
   int out_f32;                 /* C is fp32 */
+  int b_kn;                    /* B is stored K x N */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

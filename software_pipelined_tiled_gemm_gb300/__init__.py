@@ -24,7 +24,7 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "GemmError", "Plan", "matmul_nt", "load_library", "library_path",
+    "GemmError", "Plan", "matmul_nt", "matmul_nn", "load_library", "library_path",
     "gemm_plan_create", "gemm_plan_create_ex", "gemm_run", "gemm_run_host", "gemm_plan_check",
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
@@ -58,7 +58,7 @@ class GemmTuning(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
-                ("out_f32", ctypes.c_int), ("debug_fault", ctypes.c_int)]
+                ("b_kn", ctypes.c_int), ("out_f32", ctypes.c_int), ("debug_fault", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -70,7 +70,7 @@ class GemmPlanInfo(ctypes.Structure):
                 ("kernels_per_run", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("cta_group", ctypes.c_int), ("tail_tiles", ctypes.c_int64),
                 ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64),
-                ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int)]
+                ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int), ("b_kn", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -236,7 +236,7 @@ class Plan:
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
                  tile_n=0, raster_group=0, max_ctas=0, cta_group=0, tail_split=0,
-                 timeout_ns=0, out_f32=0, debug_fault=0):
+                 timeout_ns=0, b_kn=0, out_f32=0, debug_fault=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -245,7 +245,8 @@ class Plan:
         self.device = int(device)
         self._h = None
         tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
-                            int(tail_split), int(timeout_ns), int(out_f32), int(debug_fault))
+                            int(tail_split), int(timeout_ns), int(b_kn), int(out_f32),
+                            int(debug_fault))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")
@@ -296,6 +297,17 @@ _plans = {}
 _plans_lock = threading.Lock()
 
 
+def matmul_nn(A, B, epilogue=None, stages: int = 6, out=None, out_dtype=None, **tuning):
+    """C = epi(A @ B) on the current CUDA stream, B stored (K, N) row-major.
+
+    The [M, K] @ [K, N] form of the Mosaic GPU pipelining guide's example;
+    same arguments and checks as :func:`matmul_nt` otherwise."""
+    if B.dim() != 2 or A.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A must be (M, K) and B (K, N) with the same K")
+    return matmul_nt(A, B, epilogue=epilogue, stages=stages, out=out, out_dtype=out_dtype,
+                     _b_kn=True, **tuning)
+
+
 def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
              **tuning) -> Plan:
     key = (M, N, K, dtype, epilogue, stages, variant, device, tuple(sorted(tuning.items())))
@@ -317,9 +329,10 @@ def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", 
     (``out`` if given).
     """
     import torch
+    b_kn = bool(tuning.pop("_b_kn", False))
     if not (A.is_cuda and B.is_cuda):
         raise ValueError("A and B must be CUDA tensors")
-    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0 if b_kn else 1]:
         raise ValueError("A must be (M, K) and B (N, K) with the same K")
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
@@ -329,7 +342,9 @@ def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", 
         raise ValueError("A and B must be on the same device")
     dt = _torch_dtype_code(A)
     M, K = A.shape
-    N = B.shape[0]
+    N = B.shape[1] if b_kn else B.shape[0]
+    if b_kn:
+        tuning["b_kn"] = 1
     c_dtype = out_dtype if out_dtype is not None else (out.dtype if out is not None else A.dtype)
     if c_dtype not in (A.dtype, torch.float32):
         raise TypeError("C must have A's dtype or float32")

@@ -112,6 +112,7 @@ struct gemm_plan {
   unsigned long long timeout_ns = kDefaultTimeoutNs;
   int debug_fault = 0;
   int out_f32 = 0;               // C element: 0 = input type, 1 = fp32
+  int b_kn = 0;                  // B stored K x N (read MN-major)
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -288,6 +289,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
       return fail(GEMM_ERR_INVALID_ARG, "debug_fault %d not in {0, 1}", tuning->debug_fault);
     if (tuning->out_f32 < 0 || tuning->out_f32 > 1)
       return fail(GEMM_ERR_INVALID_ARG, "out_f32 %d not in {0, 1}", tuning->out_f32);
+    if (tuning->b_kn < 0 || tuning->b_kn > 1)
+      return fail(GEMM_ERR_INVALID_ARG, "b_kn %d not in {0, 1}", tuning->b_kn);
+    if (tuning->b_kn == 1 && want_split >= 2)
+      return fail(GEMM_ERR_INVALID_ARG, "narrow tail tiles are not available with b_kn = 1");
     if (tuning->timeout_ns > 0) timeout = static_cast<unsigned long long>(tuning->timeout_ns);
   }
 
@@ -380,6 +385,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->max_ctas = want_ctas;
   p->debug_fault = tuning ? tuning->debug_fault : 0;
   p->out_f32 = tuning ? tuning->out_f32 : 0;
+  p->b_kn = tuning ? tuning->b_kn : 0;
   p->bn = chosen;
   p->cg = chosen_cg;
   p->smem = chosen_smem;
@@ -446,7 +452,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         p->dp_tiles = (p->num_tiles / walkers - 1) * walkers;
         p->sk_tiles = p->num_tiles - p->dp_tiles;
       }
-    } else if (rem > 0 && (want_split >= 2 || rem * 4 <= walkers)) {
+    } else if (rem > 0 && (want_split >= 2 || rem * 4 <= walkers) &&
+               !(tuning && tuning->b_kn)) {
       int64_t S = want_split >= 2 ? want_split : std::min<int64_t>(walkers / rem, max_s);
       if (S >= 2 && S <= max_s && p->bn % S == 0) {
         p->dp_tiles = p->num_tiles - rem;
@@ -461,7 +468,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   }
   // One row of tiles streaming a large B (memory-bound): prefetch B into L2
   // in 512-byte row runs, 8 slices ahead.
-  p->prefetch_kb = (p->tiles_m == 1 && k_blocks >= 4 * kPrefetchSlices) ? 8 : 0;
+  p->prefetch_kb =
+      (p->tiles_m == 1 && k_blocks >= 4 * kPrefetchSlices && !(tuning && tuning->b_kn)) ? 8 : 0;
   const int64_t tail = p->num_tiles - p->dp_tiles;
   p->num_units = p->sk_tiles > 0 ? p->dp_tiles : p->dp_tiles + tail * p->tail_splits;
   if (p->num_units > kMaxDim) {
@@ -557,39 +565,63 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     return GEMM_OK;
   }
 
-  // Operands whose pitch or base is not 16-byte aligned go through padded scratch.
+  // Operands whose pitch or base is not 16-byte aligned go through padded
+  // scratch.  B's pitch is K (N x K) or, with b_kn, N (K x N).
   const bool padA = (K % 8) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
-  const bool padB = (K % 8) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
+  const int64_t bcols = plan->b_kn ? N : K;   // B's contiguous extent
+  const int64_t brows = plan->b_kn ? K : N;
+  const bool padB = (bcols % 8) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
   const int64_t Kp = (K + 7) / 8 * 8;
+  const int64_t Bp_cols = (bcols + 7) / 8 * 8;
   const void* effA = A;
   const void* effB = B;
   int kernels = 0;
   if (padA || padB) {
-    const size_t need = ((padA ? M : 0) + (padB ? N : 0)) * static_cast<size_t>(Kp) * 2;
-    if (need > plan->scratch_bytes) {
+    const size_t need = (padA ? static_cast<size_t>(M) * Kp : 0) +
+                        (padB ? static_cast<size_t>(brows) * Bp_cols : 0);
+    const size_t need_bytes = need * 2;
+    if (need_bytes > plan->scratch_bytes) {
       if (plan->scratch) {
         cudaError_t e = cudaFree(plan->scratch);
         plan->scratch = nullptr;
         plan->scratch_bytes = 0;
         if (e != cudaSuccess) return cuda_fail(e, "cudaFree(scratch)");
       }
-      cudaError_t e = cudaMalloc(&plan->scratch, need);
+      cudaError_t e = cudaMalloc(&plan->scratch, need_bytes);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(scratch)");
-      plan->scratch_bytes = need;
+      plan->scratch_bytes = need_bytes;
       plan->mapA_ptr = plan->mapB_ptr = nullptr;
     }
     uint16_t* Ap = padA ? plan->scratch : nullptr;
     uint16_t* Bp = padB ? plan->scratch + (padA ? M * Kp : 0) : nullptr;
-    cudaError_t e = launch_pad_operands(static_cast<const uint16_t*>(A), M, Ap,
-                                        static_cast<const uint16_t*>(B), N, Bp, K, Kp,
-                                        plan->sm_count, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
-    ++kernels;
+    cudaError_t e;
+    if (!plan->b_kn) {
+      e = launch_pad_operands(static_cast<const uint16_t*>(A), M, Ap,
+                              static_cast<const uint16_t*>(B), N, Bp, K, Kp, plan->sm_count,
+                              stream);
+      if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
+      ++kernels;
+    } else {  // rows of different length: one launch per operand
+      if (padA) {
+        e = launch_pad_operands(static_cast<const uint16_t*>(A), M, Ap, nullptr, 0, nullptr, K,
+                                Kp, plan->sm_count, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
+        ++kernels;
+      }
+      if (padB) {
+        e = launch_pad_operands(static_cast<const uint16_t*>(B), K, Bp, nullptr, 0, nullptr, N,
+                                Bp_cols, plan->sm_count, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
+        ++kernels;
+      }
+    }
     if (padA) effA = Ap;
     if (padB) effB = Bp;
   }
-  const int64_t Keff = (padA || padB) ? Kp : K;
-  // If only one operand is padded, the other's pitch is K == Kp (K % 8 == 0).
+  // A's pitch (and, for N x K B, B's): Kp when padded (K % 8 == 0 otherwise,
+  // so K == Kp); a K x N B has pitch Bp_cols when padded, else N.
+  const int64_t Keff = (padA || (padB && !plan->b_kn)) ? Kp : K;
+  const int64_t Beff_cols = plan->b_kn ? (padB ? Bp_cols : N) : Keff;
 
   const bool tma_store =
       (static_cast<size_t>(N) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
@@ -603,8 +635,12 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     plan->mapA_ptr = effA;
   }
   if (plan->mapB_ptr != effB || plan->mapK != Keff) {
-    st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
-                   static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (!plan->b_kn)
+      st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
+                     static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    else  // K x N: boxes of 64 columns x 64 K rows, read MN-major
+      st = encode_2d(&plan->tmB, plan->dtype, effB, N, K, Beff_cols, 64, kBK,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (st != GEMM_OK) return st;
     if (plan->tail_splits > 1) {
       st = encode_2d(&plan->tmBt, plan->dtype, effB, Keff, N, Keff, kBK,
@@ -655,7 +691,8 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.epilogue = static_cast<int>(plan->epi);
   prm.out_f32 = plan->out_f32;
   prm.tma_store = tma_store ? 1 : 0;
-  prm.idesc = ptx::instr_desc_f16(kBM * plan->cg, plan->bn, plan->dtype == GEMM_BF16);
+  prm.idesc = ptx::instr_desc_f16(kBM * plan->cg, plan->bn, plan->dtype == GEMM_BF16,
+                                  plan->b_kn != 0);
   prm.C = C;
   prm.ldc = N;
   prm.status = plan->d_status;
@@ -664,13 +701,14 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.tail_splits = plan->tail_splits;
   prm.num_units = static_cast<int>(plan->num_units);
   prm.idesc_tail = ptx::instr_desc_f16(kBM * plan->cg, plan->bn / plan->tail_splits,
-                                       plan->dtype == GEMM_BF16);
+                                       plan->dtype == GEMM_BF16, plan->b_kn != 0);
   // One row of tiles across the whole grid: every CTA reads the same A rows,
   // so stagger where each starts along K.
   prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
   prm.inject_fault = plan->debug_fault;
   prm.prefetch_kb = plan->prefetch_kb;
   prm.a_box_rows = static_cast<int>(a_box_rows);
+  prm.b_kn = plan->b_kn;
   prm.sk_tiles = static_cast<int>(plan->sk_tiles);
   prm.sk_ws = plan->sk_ws;
   prm.sk_flags = plan->sk_flags;
@@ -765,6 +803,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->work_units = plan->num_units;
   info->stream_k = plan->sk_tiles > 0 ? 1 : 0;
   info->out_f32 = plan->out_f32;
+  info->b_kn = plan->b_kn;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
   return GEMM_OK;
 }

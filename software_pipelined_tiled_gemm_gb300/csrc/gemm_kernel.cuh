@@ -407,13 +407,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-              ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
+              if (!p.b_kn) {
+                ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
+              } else {
+                for (int c = 0; c < b_rows / 64; ++c)  // 64 columns x 64 K rows per box
+                  ptx::tma_load_2d_pair(sa + kStageA + c * (kBK * 128), tmb, b_row + c * 64,
+                                        kb * kBK, fb);
+              }
             }
           } else {
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-              ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
+              if (!p.b_kn) {
+                ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
+              } else {
+                for (int c = 0; c < b_rows / 64; ++c)
+                  ptx::tma_load_2d(sa + kStageA + c * (kBK * 128), tmb, b_row + c * 64, kb * kBK,
+                                   full_bar(stage));
+              }
             }
           }
           issued |= 1u << stage;
@@ -459,12 +471,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after_sync();
           const uint32_t sa = sbase + stage * kStage;
           const uint64_t a_desc = ptx::smem_desc_k_sw128(sa);
-          const uint64_t b_desc = ptx::smem_desc_k_sw128(sa + kStageA);
+          // K-major B: +32 B per 16-wide K step inside the swizzled row (+2 in
+          // 16-byte units).  MN-major B: +16 K rows = +2048 B (+128).
+          const uint64_t b_desc = p.b_kn ? ptx::smem_desc_mn_sw128(sa + kStageA, kBK * 128)
+                                         : ptx::smem_desc_k_sw128(sa + kStageA);
+          const uint32_t b_step = p.b_kn ? 128u : 2u;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
             // descriptor's address field (16-byte units).
-            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, idesc,
                                 (kb | k) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)

@@ -84,6 +84,9 @@ struct Params {
   // the other 64 rows of the slot are left as they are -- they only feed
   // output rows >= M, which are never stored).
   int a_box_rows;
+  // 1: B is stored K x N (N contiguous) and read MN-major: the B map's boxes
+  // are 64 columns x 64 K rows, one per 64 columns of the CTA's B share.
+  int b_kn;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
   // copies of its first K slice (see gemm_tuning_t::debug_fault).
   int inject_fault;

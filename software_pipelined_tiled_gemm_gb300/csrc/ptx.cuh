@@ -320,14 +320,31 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory descriptor for an MN-major operand tile written by TMA with
+// 128-byte swizzling: for each block of 64 M/N elements (128 B) the K rows
+// follow each other 128 B apart (8-row swizzle atoms of 1024 B), and the
+// blocks are `block_stride` bytes apart.
+//   leading-dimension byte offset = block_stride (between 64-element MN blocks)
+//   stride-dimension byte offset  = 1024 (between 8-row K groups)
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t block_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((block_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation,
-// both operands K-major.
+// A K-major; B K-major (b_mn = false) or MN-major (b_mn = true, bit 16).
 //   bits 4-5 D format (1 = f32); bits 7-9 A format, 10-12 B format
 //   (0 = f16, 1 = bf16); bit 15/16 A/B major (0 = K); bits 17-22 N >> 3;
 //   bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n, bool bf16) {
+__host__ __device__ constexpr uint32_t instr_desc_f16(int m, int n, bool bf16, bool b_mn = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 }  // namespace ptx

@@ -18,14 +18,15 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def run_device(A: torch.Tensor, B: torch.Tensor, dtype: str, epilogue=None, stages=4,
                variant="pipelined", c_offset=0, a_offset=0, b_offset=0, fill=0xFFFF, **tuning):
-    """Run C = epi(A.B^T) on cuda:0 through gemm_run.
+    """Run C = epi(A.B^T) on cuda:0 through gemm_run (C = epi(A.B) with B of
+    shape (K, N) when tuning has b_kn=1).
 
     *_offset place the operand `offset` elements into a larger allocation (to
     exercise unaligned base addresses); C's surroundings are filled with the
     `fill` pattern and returned so callers can check nothing outside C was
     written.  Returns (C_cpu, plan_info, canary_ok)."""
     M, K = A.shape
-    N = B.shape[0]
+    N = B.shape[1] if tuning.get("b_kn") else B.shape[0]
     dev = torch.device("cuda", 0)
 
     def place(x, off):

@@ -77,7 +77,8 @@ def test_plan_create_ex_rejects_bad_tuning():
               sg.GemmTuning(0, 0, 0, -1, 0, 0), sg.GemmTuning(64, 0, 0, 2, 0, 0),
               sg.GemmTuning(0, 0, 0, 0, -2, 0),
               sg.GemmTuning(0, 0, 0, 0, 5, 0), sg.GemmTuning(0, 0, 0, 0, 0, -5),
-              sg.GemmTuning(0, 0, 0, 0, 0, 0, 2)):
+              sg.GemmTuning(0, 0, 0, 0, 0, 0, 2), sg.GemmTuning(b_kn=-1),
+              sg.GemmTuning(out_f32=3), sg.GemmTuning(tail_split=2, b_kn=1)):
         st, h = sg.gemm_plan_create_ex(64, 64, 64, 0, 0, 4, 0, 0, t)
         assert st == sg.GEMM_ERR_INVALID_ARG and h is None
 
@@ -111,6 +112,21 @@ def test_plan_class_raises_gemm_error():
     with pytest.raises(sg.GemmError) as ei:
         sg.Plan(-1, 4, 4, "f16")
     assert ei.value.status == sg.GEMM_ERR_INVALID_ARG
+
+
+def test_tuning_field_order_matches_the_header():
+    # The ctypes mirror must list gemm_tuning_t's fields in the header's order.
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct \{(.*?)\} gemm_tuning_t;", src, flags=re.S).group(1)
+    names = re.findall(r"\b(\w+);", body)
+    assert names == [f[0] for f in sg.GemmTuning._fields_]
+
+
+def test_matmul_nn_checks_shapes_on_cpu_tensors():
+    import torch
+    a = torch.zeros(4, 8, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        sg.matmul_nn(a, torch.zeros(4, 8, dtype=torch.float16))   # B must be (K, N)
 
 
 def test_matmul_nt_checks_arguments_on_cpu_tensors():
