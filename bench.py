@@ -7,6 +7,7 @@ one full GEMM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--stages S] [--variant pipelined|single_buffer]
+                  [--layout nt|nn] [--epilogue auto|none|gelu|relu] [--out-f32]
 
 --impl reference times the CPU oracle (fp64, OpenMP) on a bounded sample of
 the same workload: a block of output rows per step.
@@ -57,6 +58,17 @@ def parse():
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--tail-split", type=int, default=0,
                     help="K-splitting of the last partial wave: 0 auto, -1 off, k >= 2 forced")
+    ap.add_argument("--layout", default="nt", choices=["nt", "nn"],
+                    help="nt: B is (N, K), C = A.B^T; nn: B is (K, N), C = A.B")
+    ap.add_argument("--epilogue", default="auto", choices=["auto", "none", "gelu", "relu"],
+                    help="auto: the workload's own epilogue")
+    ap.add_argument("--out-f32", action="store_true", help="write C in fp32")
+    ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
+                    help="auto: flush L2 between steps when the operands fit in it")
+    ap.add_argument("--dist-reps", type=int, default=30,
+                    help="extra individually timed steps for the p10/p50/p90 spread")
+    ap.add_argument("--no-cublas", action="store_true",
+                    help="skip the torch.matmul (cuBLAS) context timing")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -203,11 +215,11 @@ def job_throughput(flops_per_step, steps, world_size, elapsed_ms):
     return flops_per_step * steps * world_size / (elapsed_ms * 1e-3) / 1e12
 
 
-def cpu_baseline(A, B, w, seconds, threads=0):
-    """Time the oracle (as it is) on a block of output rows of this workload."""
+def cpu_baseline(A, B, w, seconds, threads=0, epi=None):
+    """Time the oracle (as it is) on a block of output rows of this workload
+    (A is (M, K), B is (N, K))."""
     import oracle
     oracle.build()
-    epi = None if w.epilogue == "none" else "gelu"
     # calibrate on a few rows, then size the sample to about `seconds`
     probe = max(1, min(w.M, max(2, oracle.max_threads())))
     t0 = time.perf_counter()
@@ -231,7 +243,8 @@ def run_reference(args, w, ws, rank):
     import oracle
     oracle.build()
     A, B = gemm_inputs.make(w)
-    epi = None if w.epilogue == "none" else "gelu"
+    epi_name = w.epilogue if args.epilogue == "auto" else args.epilogue
+    epi = None if epi_name == "none" else epi_name
     total_steps = args.steps + args.warmup
     per_step = max(0.5, min(8.0, 150.0 / max(total_steps, 1)))
     probe = max(1, min(w.M, max(2, oracle.max_threads())))
@@ -253,7 +266,8 @@ def run_reference(args, w, ws, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "input_dtype": w.dtype,
-                   "epilogue": w.epilogue, "sample_rows_per_step": rows},
+                   "epilogue": epi_name, "layout": args.layout,
+                   "sample_rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
                          "kind": "oracle",
                          "sample": "%d of %d output rows per step (all columns, full K)" % (rows, w.M)},
@@ -285,18 +299,27 @@ def main():
         if ws > 1:
             dist.barrier()
 
-    epi = None if w.epilogue == "none" else "gelu"
+    epi_name = w.epilogue if args.epilogue == "auto" else args.epilogue
+    epi = None if epi_name == "none" else epi_name
     if args.variant == "single_buffer":
         args.stages = 1
+    nn = args.layout == "nn"
+    tuning = dict(tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group,
+                  tail_split=args.tail_split, b_kn=1 if nn else 0,
+                  out_f32=1 if args.out_f32 else 0)
     A_cpu, B_cpu = gemm_inputs.make(w)
+    if nn:  # the same draw, stored (K, N)
+        B_cpu = B_cpu.t().contiguous()
     A, B = A_cpu.to(dev), B_cpu.to(dev)
-    C = torch.empty(w.M, w.N, dtype=A.dtype, device=dev)
-    plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
-                   tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group,
-                   tail_split=args.tail_split)
+    c_dtype = torch.float32 if args.out_f32 else A.dtype
+    C = torch.empty(w.M, w.N, dtype=c_dtype, device=dev)
+    plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local, **tuning)
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
     a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    operand_bytes = (w.M * w.K + w.N * w.K) * 2
+    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and operand_bytes <= L2_BYTES)
+    scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
@@ -307,10 +330,12 @@ def main():
         raise SystemExit("device status %d (detail %#x) after warm-up" % (ds, detail))
     info = plan.info()
 
-    # Two events bracket the timed region on the launch stream; nothing else
-    # runs on it, so the average launch duration is elapsed / steps (events
-    # between launches would also cut the programmatic-dependent-launch
-    # overlap of consecutive GEMMs).
+    # Without flushing, two events bracket the timed region on the launch
+    # stream and nothing else runs on it, so the average launch duration is
+    # elapsed / steps (events between launches would also cut the
+    # programmatic-dependent-launch overlap of consecutive GEMMs).  With
+    # flushing (operands that fit in L2), each step is bracketed by its own
+    # events and a 2 x L2 write runs between steps, outside them.
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -318,15 +343,27 @@ def main():
     barrier()
     torch.cuda.synchronize(dev)
     clocks.mark_start()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        plan.run_ptr(a_p, b_p, c_p, sptr)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    if not flush:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            plan.run_ptr(a_p, b_p, c_p, sptr)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        elapsed_ms = ev0.elapsed_time(ev1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                scrub.fill_(1)
+                e0.record(stream)
+                plan.run_ptr(a_p, b_p, c_p, sptr)
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
     clocks.mark_stop()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
     ds, detail = plan.check()
     if ds != 0:
         raise SystemExit("device status %d (detail %#x) after timed steps" % (ds, detail))
@@ -339,14 +376,51 @@ def main():
     kavg = elapsed_ms / args.steps
     achieved = flops / (kavg * 1e-3) / 1e12
 
+    # Spread of single-step device times (outside the timed region): each
+    # step bracketed by its own events, L2 flushed first when flushing.
+    dist_ms = None
+    if args.dist_reps > 0:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.dist_reps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                if flush:
+                    scrub.fill_(1)
+                e0.record(stream)
+                plan.run_ptr(a_p, b_p, c_p, sptr)
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+        q = lambda f: t[min(len(t) - 1, int(round(f * (len(t) - 1))))]  # noqa: E731
+        dist_ms = {"p10": q(0.1), "p50": q(0.5), "p90": q(0.9), "reps": len(t)}
+
+    # torch.matmul (cuBLAS) on the same operands: context only, not timed
+    # as part of this library.
+    cublas = None
+    if not args.no_cublas and epi is None and not args.out_f32:
+        bt = B if nn else B.t()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                torch.matmul(A, bt)
+            reps = 20
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for _ in range(reps):
+                torch.matmul(A, bt)
+            c1.record(stream)
+        torch.cuda.synchronize(dev)
+        cms = c0.elapsed_time(c1) / reps
+        cublas = {"tflops": 2.0 * w.M * w.N * w.K / (cms * 1e-3) / 1e12, "ms": cms,
+                  "what": "torch.matmul on the same device operands, %d back-to-back reps%s" % (
+                      reps, "" if not flush else ", no flush")}
+
     # end-to-end through the C ABI with host buffers (pinned)
     e2e = None
     if args.e2e_steps > 0:
         hA, hB = A_cpu.pin_memory(), B_cpu.pin_memory()
-        hC = torch.empty(w.M, w.N, dtype=A_cpu.dtype).pin_memory()
-        eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local,
-                        tile_n=args.tile_n, raster_group=args.raster_group,
-                        cta_group=args.cta_group, tail_split=args.tail_split)
+        hC = torch.empty(w.M, w.N, dtype=c_dtype).pin_memory()
+        eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local, **tuning)
         eplan.run_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), sptr)
         barrier()
         t0 = time.perf_counter()
@@ -356,7 +430,7 @@ def main():
         eplan.close()
         e2e = {"value": job_throughput(flops, args.e2e_steps, ws, el * 1e3), "unit": UNIT,
                "h2d_bytes_per_step": (w.M * w.K + w.N * w.K) * 2,
-               "d2h_bytes_per_step": w.M * w.N * 2}
+               "d2h_bytes_per_step": w.M * w.N * C.element_size()}
 
     peaks, peak_src = load_peaks()
     sustained = elapsed_ms > 1000.0
@@ -364,8 +438,10 @@ def main():
     peak = float(peaks.get(peak_key, FALLBACK_TFLOPS))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM))
     digest = source_digest()
-    traffic = traffic_from_profiles(w.name, digest)
-    min_bytes = 2.0 * (w.M * w.K + w.N * w.K + w.M * w.N)
+    variant_key = w.name + ("" if not nn else ":nn") + ("" if epi_name == w.epilogue else
+                                                         ":" + epi_name)
+    traffic = traffic_from_profiles(variant_key, digest)
+    min_bytes = 2.0 * (w.M * w.K + w.N * w.K) + float(w.M * w.N * C.element_size())
     # Below the ridge point (peak flops / HBM bandwidth) the GEMM is bound by
     # moving its operands once; report it against the copy bandwidth.
     if flops / min_bytes < peak * 1e12 / (hbm * 1e9):
@@ -384,7 +460,8 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
-        cpu, _ = cpu_baseline(A_cpu, B_cpu, w, args.cpu_seconds)
+        cpu, _ = cpu_baseline(A_cpu, B_cpu.t().contiguous() if nn else B_cpu, w,
+                              args.cpu_seconds, epi=epi)
 
     if rank == 0:
         line = {
@@ -394,15 +471,18 @@ def main():
             "data": "synthetic",
             "config": {
                 "workload": w.name, "M": w.M, "N": w.N, "K": w.K, "input_dtype": w.dtype,
-                "accumulate": "f32", "epilogue": w.epilogue, "variant": args.variant,
+                "accumulate": "f32", "epilogue": epi_name, "variant": args.variant,
+                "layout": args.layout, "output_dtype": "f32" if args.out_f32 else w.dtype,
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],
                 "cta_group": info["cta_group"], "tail_splits": info["tail_splits"],
                 "tail_tiles": info["tail_tiles"],
-                "l2": ("inputs larger than L2 (%d MiB of operands vs %d MiB L2); no flush"
-                       % ((w.M * w.K + w.N * w.K) * 2 >> 20, L2_BYTES >> 20))
-                if (w.M * w.K + w.N * w.K) * 2 > L2_BYTES else "operands fit in L2 (warm)",
+                "l2": ("L2 flushed (2 x %d MiB write) before every step" % (L2_BYTES >> 20))
+                if flush else
+                ("inputs larger than L2 (%d MiB of operands vs %d MiB L2); no flush"
+                 % (operand_bytes >> 20, L2_BYTES >> 20))
+                if operand_bytes > L2_BYTES else "operands fit in L2, not flushed (warm)",
                 "parallelism": "replicas" if ws > 1 else "single-gpu",
             },
             "roofline": roof,
@@ -410,6 +490,8 @@ def main():
             "e2e": e2e,
             "gpu_launches": args.steps * info["kernels_per_run"],
             "cpu_baseline": cpu,
+            "step_ms_dist": dist_ms,
+            "cublas_context": cublas,
         }
         print(json.dumps(line), flush=True)
     plan.close()

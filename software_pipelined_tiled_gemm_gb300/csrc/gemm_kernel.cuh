@@ -201,12 +201,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Epilogue functions on an fp32 accumulator value: 0 identity, 1 tanh-GELU,
-// 2 ReLU (max(x, 0), with -0 and NaN giving +0).
-__device__ __forceinline__ float apply_epilogue(float x, int epilogue) {
-  if (epilogue == 1) return gelu_tanh(x);
-  if (epilogue == 2) return x > 0.0f ? x : 0.0f;
-  return x;
+template <int EPI>
+__device__ __forceinline__ void apply_epilogue32(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float x = __uint_as_float(r[j]);
+    if constexpr (EPI == 1) x = gelu_tanh(x);
+    if constexpr (EPI == 2) x = x > 0.0f ? x : 0.0f;
+    r[j] = __float_as_uint(x);
+  }
 }
 
 // Store one 32-row x 128-byte block of C held as 32 words per lane (lane =
@@ -283,7 +286,8 @@ __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params
 // kSplit: this instance can run narrow tail tiles (BN / tail_splits wide,
 // B loaded through tmBt) and stream-K pieces; the instance used by plans
 // that need neither has that code compiled out.
-template <int BN, int CG, bool kSplit>
+// kKN: B is stored K x N and read MN-major (see Params::b_kn).
+template <int BN, int CG, bool kSplit, bool kKN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-              if (!p.b_kn) {
+              if constexpr (!kKN) {
                 ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
               } else {
                 for (int c = 0; c < b_rows / 64; ++c)  // 64 columns x 64 K rows per box
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-              if (!p.b_kn) {
+              if constexpr (!kKN) {
                 ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
               } else {
                 for (int c = 0; c < b_rows / 64; ++c)
@@ -473,9 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a_desc = ptx::smem_desc_k_sw128(sa);
           // K-major B: +32 B per 16-wide K step inside the swizzled row (+2 in
           // 16-byte units).  MN-major B: +16 K rows = +2048 B (+128).
-          const uint64_t b_desc = p.b_kn ? ptx::smem_desc_mn_sw128(sa + kStageA, kBK * 128)
-                                         : ptx::smem_desc_k_sw128(sa + kStageA);
-          const uint32_t b_step = p.b_kn ? 128u : 2u;
+          const uint64_t b_desc = kKN ? ptx::smem_desc_mn_sw128(sa + kStageA, kBK * 128)
+                                      : ptx::smem_desc_k_sw128(sa + kStageA);
+          constexpr uint32_t b_step = kKN ? 128u : 2u;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the
@@ -595,24 +599,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // Epilogue function on the fp32 accumulator values.
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            r0[j] = __float_as_uint(apply_epilogue(__uint_as_float(r0[j]), p.epilogue));
-            r1[j] = __float_as_uint(apply_epilogue(__uint_as_float(r1[j]), p.epilogue));
+          if (p.epilogue == 1) {
+            apply_epilogue32<1>(r0);
+            apply_epilogue32<1>(r1);
+          } else if (p.epilogue == 2) {
+            apply_epilogue32<2>(r0);
+            apply_epilogue32<2>(r1);
           }
-          if (!p.out_f32) {
-            // Round to fp16/bf16: 64 columns = 32 packed words = one 128-byte row.
+          const int halves = p.out_f32 ? 2 : 1;
+#pragma unroll 1
+          for (int h = 0; h < halves; ++h) {
             uint32_t pk[32];
+            if (!p.out_f32) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              pk[j] = pack2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), bf16);
-              pk[16 + j] = pack2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), bf16);
+              for (int j = 0; j < 16; ++j) {
+                pk[j] = pack2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), bf16);
+                pk[16 + j] = pack2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), bf16);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) pk[j] = h ? r1[j] : r0[j];
             }
-            store_rows(pk, p, tmC, my_stage, buf, lane, row0, col0, 2);
-          } else {
-            // fp32 output: each 32-column half is one 128-byte row.
-            store_rows(r0, p, tmC, my_stage, buf, lane, row0, col0, 4);
-            store_rows(r1, p, tmC, my_stage, buf, lane, row0, col0 + 32, 4);
+            store_rows(pk, p, tmC, my_stage, buf, lane, row0, col0 + 32 * h, p.out_f32 ? 4 : 2);
           }
         }
       }
