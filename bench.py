@@ -396,24 +396,38 @@ def main():
 
     # torch.matmul (cuBLAS) on the same operands: context only, not timed
     # as part of this library.
+    # Same protocol as the timed region: back to back between two events, or
+    # (when flushing) each rep after an L2 flush, bracketed by its own events.
     cublas = None
     if not args.no_cublas and epi is None and not args.out_f32:
         bt = B if nn else B.t()
+        reps = 20
         with torch.cuda.stream(stream):
             for _ in range(3):
                 torch.matmul(A, bt)
-            reps = 20
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            for _ in range(reps):
-                torch.matmul(A, bt)
-            c1.record(stream)
+            if not flush:
+                c0 = torch.cuda.Event(enable_timing=True)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(reps):
+                    torch.matmul(A, bt)
+                c1.record(stream)
+            else:
+                cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(reps)]
+                for e0, e1 in cevs:
+                    scrub.fill_(1)
+                    e0.record(stream)
+                    torch.matmul(A, bt)
+                    e1.record(stream)
         torch.cuda.synchronize(dev)
-        cms = c0.elapsed_time(c1) / reps
+        if not flush:
+            cms = c0.elapsed_time(c1) / reps
+        else:
+            cms = sum(e0.elapsed_time(e1) for e0, e1 in cevs) / reps
         cublas = {"tflops": 2.0 * w.M * w.N * w.K / (cms * 1e-3) / 1e12, "ms": cms,
-                  "what": "torch.matmul on the same device operands, %d back-to-back reps%s" % (
-                      reps, "" if not flush else ", no flush")}
+                  "what": "torch.matmul on the same device operands, %d reps, %s" % (
+                      reps, "L2 flushed before each" if flush else "back to back")}
 
     # end-to-end through the C ABI with host buffers (pinned)
     e2e = None

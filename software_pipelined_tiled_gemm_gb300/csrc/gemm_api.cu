@@ -165,6 +165,32 @@ gemm_status_t encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* base, int
   return GEMM_OK;
 }
 
+// K x N B (row pitch `cols` elements, `rows` rows; cols % 64 == 0 and
+// rows % 8 == 0) viewed as (64 columns, 8 rows, cols / 64 column blocks,
+// rows / 8 row groups), box (64, 8, blocks, 8): one box is a 64-row K slice
+// of `blocks` 64-column blocks, written to shared memory as 1024-byte atoms
+// in the order [row group][column block].
+gemm_status_t encode_b_kn(CUtensorMap* map, gemm_dtype_t dt, const void* base, int64_t cols,
+                          int64_t rows, uint32_t blocks) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[4] = {64u, 8u, static_cast<cuuint64_t>(cols / 64),
+                              static_cast<cuuint64_t>(rows / 8)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(cols) * 2u, 128u,
+                                 static_cast<cuuint64_t>(cols) * 16u};
+  const cuuint32_t box[4] = {64u, 8u, blocks, static_cast<cuuint32_t>(kBK / 8)};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t =
+      dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(map, t, 4, const_cast<void*>(base), dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled (K x N B) failed (CUresult %d)",
+                static_cast<int>(r));
+  return GEMM_OK;
+}
+
 // fp32 C: 2-D map with 4-byte elements, 128-byte swizzle (box rows of 128 B).
 gemm_status_t encode_2d_f32(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
                             int64_t pitch_elems, uint32_t box_inner, uint32_t box_rows) {
@@ -439,7 +465,11 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     const int64_t ring = static_cast<int64_t>(stages) *
                          (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
     const bool sk_fits = ring >= static_cast<int64_t>(kEpiWarps) * 32 * p->bn * 4;
-    const bool sk_ok = rem > 0 && p->num_tiles >= walkers && sk_fits && k_blocks >= 2;
+    // Automatic stream-K needs long tiles: exchanging one partial costs about
+    // as much as a few K slices, so with short K it loses more than the idle
+    // part of the last wave (16896 x 512 x 640: 26 us with, 19 us without).
+    const bool sk_ok = rem > 0 && p->num_tiles >= walkers && sk_fits &&
+                       k_blocks >= (want_split == 1 ? 2 : kStreamKMinKBlocks);
     const int max_s = std::min(kMaxTailSplits, p->bn / kStoreCols);
     if (want_split == 1 || (want_split == 0 && sk_ok)) {
       if (!sk_ok && want_split == 1 && rem > 0) {
@@ -566,19 +596,26 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   }
 
   // Operands whose pitch or base is not 16-byte aligned go through padded
-  // scratch.  B's pitch is K (N x K) or, with b_kn, N (K x N).
+  // scratch.  B's pitch is K (N x K) or, with b_kn, N (K x N).  A K x N B is
+  // read through a 4-D view whose 64-column blocks and 8-row groups must lie
+  // inside the array, so it is also staged unless N % 64 == 0 and K % 8 == 0
+  // (scratch: pitch rounded up to 64 columns, rows up to a multiple of 8,
+  // the extra columns and rows zero).
   const bool padA = (K % 8) != 0 || (reinterpret_cast<uintptr_t>(A) & 15u) != 0;
   const int64_t bcols = plan->b_kn ? N : K;   // B's contiguous extent
   const int64_t brows = plan->b_kn ? K : N;
-  const bool padB = (bcols % 8) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
+  const int64_t bcol_mult = plan->b_kn ? 64 : 8;
+  const bool padB = (bcols % bcol_mult) != 0 || (plan->b_kn && (K % 8) != 0) ||
+                    (reinterpret_cast<uintptr_t>(B) & 15u) != 0;
   const int64_t Kp = (K + 7) / 8 * 8;
-  const int64_t Bp_cols = (bcols + 7) / 8 * 8;
+  const int64_t Bp_cols = (bcols + bcol_mult - 1) / bcol_mult * bcol_mult;
+  const int64_t Bp_rows = plan->b_kn ? Kp : brows;
   const void* effA = A;
   const void* effB = B;
   int kernels = 0;
   if (padA || padB) {
     const size_t need = (padA ? static_cast<size_t>(M) * Kp : 0) +
-                        (padB ? static_cast<size_t>(brows) * Bp_cols : 0);
+                        (padB ? static_cast<size_t>(Bp_rows) * Bp_cols : 0);
     const size_t need_bytes = need * 2;
     if (need_bytes > plan->scratch_bytes) {
       if (plan->scratch) {
@@ -613,6 +650,11 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
                                 Bp_cols, plan->sm_count, stream);
         if (e != cudaSuccess) return cuda_fail(e, "pad kernel launch");
         ++kernels;
+        if (Bp_rows > K) {  // zero rows up to the next multiple of 8
+          e = cudaMemsetAsync(Bp + K * Bp_cols, 0,
+                              static_cast<size_t>(Bp_rows - K) * Bp_cols * 2, stream);
+          if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(B row padding)");
+        }
       }
     }
     if (padA) effA = Ap;
@@ -622,6 +664,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   // so K == Kp); a K x N B has pitch Bp_cols when padded, else N.
   const int64_t Keff = (padA || (padB && !plan->b_kn)) ? Kp : K;
   const int64_t Beff_cols = plan->b_kn ? (padB ? Bp_cols : N) : Keff;
+  const int64_t Beff_rows = plan->b_kn ? (padB ? Bp_rows : K) : N;
 
   const bool tma_store =
       (static_cast<size_t>(N) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
@@ -638,9 +681,9 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     if (!plan->b_kn)
       st = encode_2d(&plan->tmB, plan->dtype, effB, Keff, N, Keff, kBK,
                      static_cast<uint32_t>(plan->bn / plan->cg), CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-    else  // K x N: boxes of 64 columns x 64 K rows, read MN-major
-      st = encode_2d(&plan->tmB, plan->dtype, effB, N, K, Beff_cols, 64, kBK,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    else
+      st = encode_b_kn(&plan->tmB, plan->dtype, effB, Beff_cols, Beff_rows,
+                       static_cast<uint32_t>(plan->bn / plan->cg / 64));
     if (st != GEMM_OK) return st;
     if (plan->tail_splits > 1) {
       st = encode_2d(&plan->tmBt, plan->dtype, effB, Keff, N, Keff, kBK,

@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
   constexpr int kBRows = BN / CG;                    // B rows this CTA loads
   constexpr uint32_t kStageB = kBRows * kBK * 2;
+  constexpr uint32_t kBBlocks = kBRows / 64;           // 64-column blocks of a K x N B slot
   constexpr uint32_t kStage = kStageA + kStageB;     // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
   constexpr uint32_t kWarpPartial = 32u * BN * 4u;   // fp32 partial of one epilogue warp
@@ -411,25 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-              if constexpr (!kKN) {
+              if constexpr (!kKN)
                 ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
-              } else {
-                for (int c = 0; c < b_rows / 64; ++c)  // 64 columns x 64 K rows per box
-                  ptx::tma_load_2d_pair(sa + kStageA + c * (kBK * 128), tmb, b_row + c * 64,
-                                        kb * kBK, fb);
-              }
+              else  // (64 columns, 8 K rows, column blocks, K groups of 8)
+                ptx::tma_load_4d_pair(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8), fb);
             }
           } else {
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-              if constexpr (!kKN) {
+              if constexpr (!kKN)
                 ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
-              } else {
-                for (int c = 0; c < b_rows / 64; ++c)
-                  ptx::tma_load_2d(sa + kStageA + c * (kBK * 128), tmb, b_row + c * 64, kb * kBK,
-                                   full_bar(stage));
-              }
+              else
+                ptx::tma_load_4d(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8),
+                                 full_bar(stage));
             }
           }
           issued |= 1u << stage;
@@ -476,10 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = sbase + stage * kStage;
           const uint64_t a_desc = ptx::smem_desc_k_sw128(sa);
           // K-major B: +32 B per 16-wide K step inside the swizzled row (+2 in
-          // 16-byte units).  MN-major B: +16 K rows = +2048 B (+128).
-          const uint64_t b_desc = kKN ? ptx::smem_desc_mn_sw128(sa + kStageA, kBK * 128)
-                                      : ptx::smem_desc_k_sw128(sa + kStageA);
-          constexpr uint32_t b_step = kKN ? 128u : 2u;
+          // 16-byte units).  MN-major B (atoms [K group][column block], the
+          // column blocks of one K group adjacent): +2 K groups per step.
+          const uint64_t b_desc =
+              kKN ? ptx::smem_desc_mn_sw128(sa + kStageA, 1024u, kBBlocks * 1024u)
+                  : ptx::smem_desc_k_sw128(sa + kStageA);
+          constexpr uint32_t b_step = kKN ? 2u * kBBlocks * 1024u / 16u : 2u;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             // +32 bytes along K inside the 128-byte swizzled row = +2 in the

@@ -21,8 +21,9 @@ constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
 
-constexpr int kMaxTailSplits = 4;
-constexpr int kPrefetchSlices = 4;   // K slices per L2 prefetch box (4 x 128 B per row)    // narrow tiles a tail tile may be cut into (N >= 64 each)
+constexpr int kMaxTailSplits = 4;     // narrow tiles a tail tile may be cut into (N >= 64 each)
+constexpr int kPrefetchSlices = 4;    // K slices per L2 prefetch box (4 x 128 B per row)
+constexpr int kStreamKMinKBlocks = 32;  // automatic stream-K only for K >= 32 slices
 
 // Where a device-side wait ran out (status word [1]): role << 16 | wait id.
 constexpr int kDetailProducerEmpty = (1 << 16) | 1;
@@ -84,8 +85,10 @@ struct Params {
   // the other 64 rows of the slot are left as they are -- they only feed
   // output rows >= M, which are never stored).
   int a_box_rows;
-  // 1: B is stored K x N (N contiguous) and read MN-major: the B map's boxes
-  // are 64 columns x 64 K rows, one per 64 columns of the CTA's B share.
+  // 1: B is stored K x N (N contiguous) and read MN-major.  The B map is 4-D,
+  // (64 columns, 8 K rows, 64-column blocks, groups of 8 K rows), so one box
+  // lands in shared memory as 1024-byte swizzle atoms ordered [K group]
+  // [column block]: the blocks of one K group side by side.
   int b_kn;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
   // copies of its first K slice (see gemm_tuning_t::debug_fault).

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// 4-D tiled copy of the box at coordinates (c0, c1, c2, c3); the box lands in
+// shared memory with dimension 0 fastest.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 // Prefetch the 2-D box at (x, y) into L2 (no shared-memory destination).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -186,6 +197,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 4-D form of tma_load_2d_pair.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
 
@@ -321,16 +342,18 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t saddr) {
 }
 
 // Shared-memory descriptor for an MN-major operand tile written by TMA with
-// 128-byte swizzling: for each block of 64 M/N elements (128 B) the K rows
-// follow each other 128 B apart (8-row swizzle atoms of 1024 B), and the
-// blocks are `block_stride` bytes apart.
-//   leading-dimension byte offset = block_stride (between 64-element MN blocks)
-//   stride-dimension byte offset  = 1024 (between 8-row K groups)
-__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t block_stride) {
+// 128-byte swizzling.  The tile is made of 1024-byte swizzle atoms, each 8 K
+// rows of 64 M/N elements (128 B per row):
+//   leading-dimension byte offset `lbo` = distance between atoms that are
+//     neighbours along M/N (the next 64 elements),
+//   stride-dimension byte offset `sbo` = distance between atoms that are
+//     neighbours along K (the next 8 rows).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo,
+                                                       uint32_t sbo) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((block_stride >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1u) << 46;
   d |= static_cast<uint64_t>(2u) << 61;
   return d;

@@ -78,10 +78,14 @@ def test_nn_bf16_bit_exact():
 
 
 @pytest.mark.parametrize("shape", [(1, 8, 8), (129, 130, 72), (255, 257, 136), (300, 203, 8),
-                                   (257, 385, 263), (513, 1001, 1000), (64, 66, 4096)])
+                                   (257, 385, 263), (513, 1001, 1000), (64, 66, 4096),
+                                   (200, 256, 100), (256, 512, 1000), (130, 192, 72)])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_nn_edge_shapes(shape, dtype):
-    # N % 8 != 0 pads B's rows (its pitch is N); K % 8 != 0 pads A.
+    # B (K x N) is read in 64-column blocks and 8-row groups: N % 64 != 0 or
+    # K % 8 != 0 stage it in padded scratch (K % 8 != 0 also pads A); N and K
+    # multiples of 64 and 8 but not of the tile read it in place, the
+    # partial K slice and column tiles zero-filled by the copy engine.
     M, N, K = shape
     A, B = gemm_inputs.custom(M, N, K, dtype=dtype, seed=M * 7 + N * 3 + K)
     C, info, canary = gu.run_device(A, _kn(B), dtype, b_kn=1)

@@ -416,6 +416,15 @@ def test_auto_tail_split_choice():
     p = sg.Plan(8192, 8192, 8192, "f16", stages=1, variant="single_buffer")
     assert p.info()["stream_k"] == 0 and p.info()["tail_splits"] == 1
     p.close()
+    # short K (the Mosaic guide's 16896 x 512 x 640: 10 K slices per tile):
+    # no automatic stream-K, whose partial exchange would cost more than the
+    # idle part of the last wave; forced stream-K still works there.
+    p = sg.Plan(16896, 512, 640, "f16", stages=6)
+    assert p.info()["stream_k"] == 0 and p.info()["tail_splits"] == 1
+    p.close()
+    p = sg.Plan(16896, 512, 640, "f16", stages=6, cta_group=2, tail_split=1)
+    assert p.info()["stream_k"] == 1
+    p.close()
 
 
 # ------------------------------------------------------------ stream-K --
