@@ -751,6 +751,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.inject_fault = plan->debug_fault;
   prm.prefetch_kb = plan->prefetch_kb;
   prm.a_box_rows = static_cast<int>(a_box_rows);
+  prm.b_stream = (plan->tiles_m == 1 && plan->cg == 1) ? 1 : 0;
   prm.b_kn = plan->b_kn;
   prm.sk_tiles = static_cast<int>(plan->sk_tiles);
   prm.sk_ws = plan->sk_ws;

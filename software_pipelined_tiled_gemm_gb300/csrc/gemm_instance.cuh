@@ -1,8 +1,9 @@
 // gemm_instance.cuh -- defines the launchers of one kernel shape.  Each shape
-// has four instances: with or without the narrow-tile / stream-K code
-// (kSplit), and for B stored N x K or K x N (kKN); the launcher picks the one
-// the plan's parameters need, so no instance carries a runtime branch on
-// either choice in its copy and MMA loops.
+// has four instances -- with or without the narrow-tile / stream-K code
+// (kSplit), for B stored N x K or K x N (kKN) -- and single-CTA shapes four
+// more whose B copies are marked evict-first (kStream); the launcher picks the
+// one the plan's parameters need, so no instance carries a runtime branch on
+// these choices in its copy and MMA loops.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -14,24 +15,55 @@ template <int BN, int CG>
 cudaError_t set_smem_all(size_t smem) {
   const int bytes = static_cast<int>(smem);
   const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false>, attr, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false>, attr, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true>, attr, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true>, attr, bytes);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false, false>, attr, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false, false>, attr, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true, false>, attr, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true, false>, attr, bytes);
+  if constexpr (CG == 1) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false, true>, attr, bytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false, true>, attr, bytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true, true>, attr, bytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true, true>, attr, bytes);
+  }
   return e;
 }
 
+template <int BN, int CG, bool kStream>
+cudaError_t launch_layout(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
+                          const CUtensorMap& b, const CUtensorMap& bt, const CUtensorMap& c,
+                          const CUtensorMap& bp, const Params& p) {
+  const bool split = p.tail_splits > 1 || p.sk_tiles > 0;
+  if (p.b_kn) {
+    if (split)
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, true, kStream>, a, b, bt, c,
+                                bp, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, true, kStream>, a, b, bt, c, bp,
+                              p);
+  }
+  if (split)
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, false, kStream>, a, b, bt, c, bp,
+                              p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, false, kStream>, a, b, bt, c, bp,
+                            p);
+}
+
+// Picks the instance for the plan: narrow / stream-K code or not, B layout,
+// and (single CTAs only) whether B's copies are marked evict-first.
 template <int BN, int CG>
 cudaError_t launch_instance(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
                             const CUtensorMap& b, const CUtensorMap& bt, const CUtensorMap& c,
                             const CUtensorMap& bp, const Params& p) {
-  const bool split = p.tail_splits > 1 || p.sk_tiles > 0;
-  if (p.b_kn) {
-    if (split) return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, true>, a, b, bt, c, bp, p);
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, true>, a, b, bt, c, bp, p);
+  if constexpr (CG == 1) {
+    if (p.b_stream) return launch_layout<BN, CG, true>(cfg, a, b, bt, c, bp, p);
   }
-  if (split) return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, false>, a, b, bt, c, bp, p);
-  return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, false>, a, b, bt, c, bp, p);
+  return launch_layout<BN, CG, false>(cfg, a, b, bt, c, bp, p);
 }
 
 // Launch configuration: `grid` CTAs of kThreads threads, programmatic
@@ -81,7 +113,8 @@ inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int 
     cudaLaunchConfig_t cfg;                                                                    \
     cudaLaunchAttribute attr[2];                                                               \
     make_config(cfg, attr, 2, 2, smem, nullptr);                                               \
-    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false, false>, &cfg); \
+    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false, false, false>, \
+                                          &cfg);                                               \
   }                                                                                            \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,                 \
                                    const CUtensorMap& bt, const CUtensorMap& c,                \

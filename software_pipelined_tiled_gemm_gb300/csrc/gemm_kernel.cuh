@@ -287,7 +287,9 @@ __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params
 // B loaded through tmBt) and stream-K pieces; the instance used by plans
 // that need neither has that code compiled out.
 // kKN: B is stored K x N and read MN-major (see Params::b_kn).
-template <int BN, int CG, bool kSplit, bool kKN>
+// kStream: every element of B is read once, and B's copies carry an
+// evict-first L2 policy (see Params::b_stream).
+template <int BN, int CG, bool kSplit, bool kKN, bool kStream>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
@@ -373,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-slot: used at all / parity of last use
+      // B read once (a single row of tiles): evict its lines from L2 first.
+      const uint64_t pol_b = kStream ? ptx::l2_policy_evict_first() : 0;
       bool ok = true;
       UnitIter it(walker, walkers, p);
       Unit x;
@@ -412,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
+              static_assert(!kStream, "streamed B is a single-CTA instance");
               if constexpr (!kKN)
                 ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
               else  // (64 columns, 8 K rows, column blocks, K groups of 8)
@@ -421,11 +426,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
             if (!skip) {
               ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-              if constexpr (!kKN)
+              if constexpr (!kKN && !kStream)
                 ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
-              else
+              else if constexpr (!kKN)
+                ptx::tma_load_2d_hint(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage), pol_b);
+              else if constexpr (!kStream)
                 ptx::tma_load_4d(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8),
                                  full_bar(stage));
+              else
+                ptx::tma_load_4d_hint(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8),
+                                      full_bar(stage), pol_b);
             }
           }
           issued |= 1u << stage;

@@ -81,6 +81,9 @@ struct Params {
   // through a tensor map whose box spans 4 K slices (512 contiguous bytes of
   // each row): memory-bound shapes then read B in longer runs.
   int prefetch_kb;
+  // 1: every element of B is read by one CTA only (a single row of
+  // single-CTA tiles), so B's copies carry an evict-first L2 policy.
+  int b_stream;
   // Rows of the A box the copy engine writes per CTA (128, or 64 when M <= 64:
   // the other 64 rows of the slot are left as they are -- they only feed
   // output rows >= M, which are never stored).
