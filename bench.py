@@ -490,7 +490,8 @@ def main():
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],
-                "cta_group": info["cta_group"], "tail_splits": info["tail_splits"],
+                "cta_group": info["cta_group"], "k_slices_per_slot": info["k_sub"],
+                "tail_splits": info["tail_splits"],
                 "tail_tiles": info["tail_tiles"],
                 "l2": ("L2 flushed (2 x %d MiB write) before every step" % (L2_BYTES >> 20))
                 if flush else

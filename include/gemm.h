@@ -140,6 +140,8 @@ typedef struct {
   int stream_k;                /* 1: the tail_tiles are shared out stream-K */
   int out_f32;                 /* C is fp32 */
   int b_kn;                    /* B is stored K x N */
+  int k_sub;                   /* K slices of tile_k per ring slot: stages / k_sub
+                                  slots of k_sub slices each (same shared memory) */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

@@ -1,9 +1,10 @@
 // gemm_instance.cuh -- defines the launchers of one kernel shape.  Each shape
 // has four instances -- with or without the narrow-tile / stream-K code
-// (kSplit), for B stored N x K or K x N (kKN) -- and single-CTA shapes four
-// more whose B copies are marked evict-first (kStream); the launcher picks the
-// one the plan's parameters need, so no instance carries a runtime branch on
-// these choices in its copy and MMA loops.
+// (kSplit), for B stored N x K or K x N (kKN) -- and four more: for single-CTA
+// shapes with B's copies marked evict-first (kStream), for CTA pairs with two
+// K slices per ring slot (kSub).  The launcher picks the one the plan's
+// parameters need, so no instance carries a runtime branch on these choices
+// in its copy and MMA loops.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -11,59 +12,64 @@
 
 namespace spgemm {
 
-template <int BN, int CG>
-cudaError_t set_smem_all(size_t smem) {
+template <int BN, int CG, bool kStream, int kSub>
+cudaError_t set_smem_layouts(size_t smem) {
   const int bytes = static_cast<int>(smem);
   const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false, false>, attr, bytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false, kStream, kSub>, attr, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false, false>, attr, bytes);
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false, kStream, kSub>, attr, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true, false>, attr, bytes);
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true, kStream, kSub>, attr, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true, false>, attr, bytes);
+    e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true, kStream, kSub>, attr, bytes);
+  return e;
+}
+
+template <int BN, int CG>
+cudaError_t set_smem_all(size_t smem) {
+  cudaError_t e = set_smem_layouts<BN, CG, false, 1>(smem);
   if constexpr (CG == 1) {
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, false, true>, attr, bytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, false, true>, attr, bytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, false, true, true>, attr, bytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_kernel<BN, CG, true, true, true>, attr, bytes);
+    if (e == cudaSuccess) e = set_smem_layouts<BN, CG, true, 1>(smem);
+  } else {
+    if (e == cudaSuccess) e = set_smem_layouts<BN, CG, false, 2>(smem);
   }
   return e;
 }
 
-template <int BN, int CG, bool kStream>
+template <int BN, int CG, bool kStream, int kSub>
 cudaError_t launch_layout(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& bt, const CUtensorMap& c,
                           const CUtensorMap& bp, const Params& p) {
   const bool split = p.tail_splits > 1 || p.sk_tiles > 0;
   if (p.b_kn) {
     if (split)
-      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, true, kStream>, a, b, bt, c,
-                                bp, p);
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, true, kStream>, a, b, bt, c, bp,
-                              p);
+      return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, true, kStream, kSub>, a, b, bt,
+                                c, bp, p);
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, true, kStream, kSub>, a, b, bt,
+                              c, bp, p);
   }
   if (split)
-    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, false, kStream>, a, b, bt, c, bp,
-                              p);
-  return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, false, kStream>, a, b, bt, c, bp,
-                            p);
+    return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, true, false, kStream, kSub>, a, b, bt,
+                              c, bp, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tn_kernel<BN, CG, false, false, kStream, kSub>, a, b, bt, c,
+                            bp, p);
 }
 
 // Picks the instance for the plan: narrow / stream-K code or not, B layout,
-// and (single CTAs only) whether B's copies are marked evict-first.
+// evict-first B copies (single CTAs only) and two K slices per ring slot
+// (CTA pairs only).
 template <int BN, int CG>
 cudaError_t launch_instance(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
                             const CUtensorMap& b, const CUtensorMap& bt, const CUtensorMap& c,
                             const CUtensorMap& bp, const Params& p) {
   if constexpr (CG == 1) {
-    if (p.b_stream) return launch_layout<BN, CG, true>(cfg, a, b, bt, c, bp, p);
+    if (p.b_stream) return launch_layout<BN, CG, true, 1>(cfg, a, b, bt, c, bp, p);
+  } else {
+    if (p.k_sub == 2) return launch_layout<BN, CG, false, 2>(cfg, a, b, bt, c, bp, p);
   }
-  return launch_layout<BN, CG, false>(cfg, a, b, bt, c, bp, p);
+  return launch_layout<BN, CG, false, 1>(cfg, a, b, bt, c, bp, p);
 }
 
 // Launch configuration: `grid` CTAs of kThreads threads, programmatic
@@ -113,8 +119,8 @@ inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int 
     cudaLaunchConfig_t cfg;                                                                    \
     cudaLaunchAttribute attr[2];                                                               \
     make_config(cfg, attr, 2, 2, smem, nullptr);                                               \
-    return cudaOccupancyMaxActiveClusters(clusters, gemm_tn_kernel<BN, 2, false, false, false>, \
-                                          &cfg);                                               \
+    return cudaOccupancyMaxActiveClusters(clusters,                                            \
+                                          gemm_tn_kernel<BN, 2, false, false, false, 1>, &cfg); \
   }                                                                                            \
   cudaError_t gemm_launch_pair##BN(const CUtensorMap& a, const CUtensorMap& b,                 \
                                    const CUtensorMap& bt, const CUtensorMap& c,                \

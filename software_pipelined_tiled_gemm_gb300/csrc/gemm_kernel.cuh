@@ -289,16 +289,21 @@ __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params
 // kKN: B is stored K x N and read MN-major (see Params::b_kn).
 // kStream: every element of B is read once, and B's copies carry an
 // evict-first L2 policy (see Params::b_stream).
-template <int BN, int CG, bool kSplit, bool kKN, bool kStream>
+// kSub: 64-wide K slices per ring slot.  With 2, one full/empty barrier
+// round trip covers 8 MMAs instead of 4 (the slot holds two slices of A and
+// two of B side by side); p.stages and p.k_blocks count slots.
+template <int BN, int CG, bool kSplit, bool kKN, bool kStream, int kSub>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmBp, const Params p) {
   static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+  static_assert(kSub == 1 || kSub == 2, "one or two K slices per slot");
   constexpr int kBRows = BN / CG;                    // B rows this CTA loads
-  constexpr uint32_t kStageB = kBRows * kBK * 2;
-  constexpr uint32_t kBBlocks = kBRows / 64;           // 64-column blocks of a K x N B slot
-  constexpr uint32_t kStage = kStageA + kStageB;     // bytes per slot, this CTA
+  constexpr uint32_t kStageB = kBRows * kBK * 2;     // B bytes of one K slice
+  constexpr uint32_t kBBlocks = kBRows / 64;           // 64-column blocks of a K x N B slice
+  constexpr uint32_t kSlotA = kStageA * kSub;        // A part of a slot
+  constexpr uint32_t kStage = kSlotA + kStageB * kSub;  // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
   constexpr uint32_t kWarpPartial = 32u * BN * 4u;   // fp32 partial of one epilogue warp
 
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
         const uint32_t bytes =
             (static_cast<uint32_t>(p.a_box_rows) * kBK * 2u + static_cast<uint32_t>(b_rows) * kBK * 2u) *
-            CG;
+            CG * kSub;
         const int nk = x.k1 - x.k0;
         const int kr = k_start(x, walker, walkers, p);
         for (int i = 0, kb = x.k0 + kr; i < nk; ++i, kb = (kb + 1 == x.k1) ? x.k0 : kb + 1) {
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (p.prefetch_kb > 0 && ((kb - x.k0) & (kPrefetchSlices - 1)) == 0) {
+          if (kSub == 1 && p.prefetch_kb > 0 && ((kb - x.k0) & (kPrefetchSlices - 1)) == 0) {
             // L2 prefetch of this unit's B rows, prefetch_kb slices ahead (wrapping
             // with the rotated K loop), 4 slices per request.
             int pk = kb + p.prefetch_kb;
@@ -414,28 +419,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             // leader announces the bytes (of both CTAs).
             const uint32_t fb = ptx::map_shared_rank(full_bar(stage), 0);
             if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-            if (!skip) {
-              ptx::tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
-              static_assert(!kStream, "streamed B is a single-CTA instance");
+            static_assert(!kStream, "streamed B is a single-CTA instance");
+#pragma unroll
+            for (int sub = 0; sub < kSub; ++sub) {
+              if (skip) break;
+              const int kx = (kb * kSub + sub) * kBK;  // first K element of this slice
+              const uint32_t da = sa + sub * kStageA, db = sa + kSlotA + sub * kStageB;
+              ptx::tma_load_2d_pair(da, &tmA, kx, a_row, fb);
               if constexpr (!kKN)
-                ptx::tma_load_2d_pair(sa + kStageA, tmb, kb * kBK, b_row, fb);
+                ptx::tma_load_2d_pair(db, tmb, kx, b_row, fb);
               else  // (64 columns, 8 K rows, column blocks, K groups of 8)
-                ptx::tma_load_4d_pair(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8), fb);
+                ptx::tma_load_4d_pair(db, tmb, 0, 0, b_row / 64, kx / 8, fb);
             }
           } else {
             ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-            if (!skip) {
-              ptx::tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
+#pragma unroll
+            for (int sub = 0; sub < kSub; ++sub) {
+              if (skip) break;
+              const int kx = (kb * kSub + sub) * kBK;
+              const uint32_t da = sa + sub * kStageA, db = sa + kSlotA + sub * kStageB;
+              ptx::tma_load_2d(da, &tmA, kx, a_row, full_bar(stage));
               if constexpr (!kKN && !kStream)
-                ptx::tma_load_2d(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage));
+                ptx::tma_load_2d(db, tmb, kx, b_row, full_bar(stage));
               else if constexpr (!kKN)
-                ptx::tma_load_2d_hint(sa + kStageA, tmb, kb * kBK, b_row, full_bar(stage), pol_b);
+                ptx::tma_load_2d_hint(db, tmb, kx, b_row, full_bar(stage), pol_b);
               else if constexpr (!kStream)
-                ptx::tma_load_4d(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8),
-                                 full_bar(stage));
+                ptx::tma_load_4d(db, tmb, 0, 0, b_row / 64, kx / 8, full_bar(stage));
               else
-                ptx::tma_load_4d_hint(sa + kStageA, tmb, 0, 0, b_row / 64, kb * (kBK / 8),
-                                      full_bar(stage), pol_b);
+                ptx::tma_load_4d_hint(db, tmb, 0, 0, b_row / 64, kx / 8, full_bar(stage), pol_b);
             }
           }
           issued |= 1u << stage;
@@ -485,15 +496,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 16-byte units).  MN-major B (atoms [K group][column block], the
           // column blocks of one K group adjacent): +2 K groups per step.
           const uint64_t b_desc =
-              kKN ? ptx::smem_desc_mn_sw128(sa + kStageA, 1024u, kBBlocks * 1024u)
-                  : ptx::smem_desc_k_sw128(sa + kStageA);
+              kKN ? ptx::smem_desc_mn_sw128(sa + kSlotA, 1024u, kBBlocks * 1024u)
+                  : ptx::smem_desc_k_sw128(sa + kSlotA);
           constexpr uint32_t b_step = kKN ? 2u * kBBlocks * 1024u / 16u : 2u;
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // +32 bytes along K inside the 128-byte swizzled row = +2 in the
-            // descriptor's address field (16-byte units).
-            ptx::mma_f16_ss<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, idesc,
-                                (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kSub * (kBK / kUmmaK); ++k) {
+            // Within a slice, +32 bytes along K inside the 128-byte swizzled
+            // row = +2 in the descriptor's address field (16-byte units); the
+            // second slice of a slot starts kStageA (A) / kStageB (B) later.
+            // K x N B: the slices' row groups follow each other, +2 groups
+            // per step throughout.
+            const uint32_t sub = static_cast<uint32_t>(k) / 4u, kk = static_cast<uint32_t>(k) % 4u;
+            const uint64_t ad = a_desc + sub * (kStageA / 16u) + 2u * kk;
+            const uint64_t bd = kKN ? b_desc + b_step * static_cast<uint32_t>(k)
+                                    : b_desc + sub * (kStageB / 16u) + 2u * kk;
+            ptx::mma_f16_ss<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           if constexpr (CG == 2)
             ptx::mma_commit_multicast_pair(empty_bar(stage), 0x3);

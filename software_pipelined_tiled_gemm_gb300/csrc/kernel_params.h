@@ -40,8 +40,8 @@ struct Params {
   int K;                 // reduction length seen by the tensor maps (padded when staged)
   int tiles_m, tiles_n;
   int num_tiles;
-  int k_blocks;          // ceil(K / kBK)
-  int stages;            // ring depth, 1..kMaxStages
+  int k_blocks;          // ceil(K / (kBK * k_sub)): ring slots of K per tile
+  int stages;            // ring depth in slots, 1..kMaxStages
   int num_acc;           // TMEM accumulators, 1 or 2
   int tmem_cols;         // allocated TMEM columns (power of two >= 32)
   int raster_group;      // tile rows per raster group
@@ -93,6 +93,8 @@ struct Params {
   // lands in shared memory as 1024-byte swizzle atoms ordered [K group]
   // [column block]: the blocks of one K group side by side.
   int b_kn;
+  // 64-wide K slices per ring slot (1 or 2); stages and k_blocks count slots.
+  int k_sub;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
   // copies of its first K slice (see gemm_tuning_t::debug_fault).
   int inject_fault;
