@@ -142,6 +142,8 @@ typedef struct {
   int b_kn;                    /* B is stored K x N */
   int k_sub;                   /* K slices of tile_k per ring slot: stages / k_sub
                                   slots of k_sub slices each (same shared memory) */
+  int host_panels;             /* row panels gemm_run_host pipelines its copies in
+                                  (0 before the first pipelined call) */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.
@@ -171,10 +173,19 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
                        gemm_epilogue_t epi, int stages, void* stream);
 
 /* End-to-end call with HOST buffers: copies hA (M*K) and hB (N*K) to
- * plan-owned device buffers on `stream`, runs the GEMM, copies C back to hC
+ * plan-owned device buffers, runs the GEMM on `stream`, copies C back to hC
  * (M*N) and synchronises `stream` before returning.  Pinned host memory gives
  * asynchronous copies; pageable memory works too.  The first call allocates
- * the device buffers. */
+ * the device buffers.
+ *
+ * Problems with at least 32 MiB of copies and M >= 2048 run as 2-4 row
+ * panels so that copies overlap the GEMM.  B comes in first, split over two
+ * plan-owned copy streams.  The panels of A follow, alternating between
+ * them.  Each panel's GEMM runs on `stream` as soon as its rows are in,
+ * through a panel plan of its own.  Its rows of C go back on a third copy
+ * stream while the next panel computes.  The copy streams wait for the work
+ * already queued on `stream`, and the call returns after all of them
+ * finish.  gemm_plan_check also reports the panel plans' device status. */
 gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, void* hC,
                             int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                             gemm_epilogue_t epi, int stages, void* stream);

@@ -71,7 +71,7 @@ class GemmPlanInfo(ctypes.Structure):
                 ("cta_group", ctypes.c_int), ("tail_tiles", ctypes.c_int64),
                 ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64),
                 ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int), ("b_kn", ctypes.c_int),
-                ("k_sub", ctypes.c_int)]
+                ("k_sub", ctypes.c_int), ("host_panels", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

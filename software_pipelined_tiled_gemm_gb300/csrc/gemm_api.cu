@@ -91,6 +91,12 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 
 }  // namespace
 
+// gemm_run_host splits problems of at least kHostPanelMinBytes of copies into
+// up to kHostPanelsMax row panels of at least kHostPanelMinRows rows.
+constexpr int kHostPanelsMax = 4;
+constexpr int64_t kHostPanelMinRows = 1024;
+constexpr size_t kHostPanelMinBytes = 32u << 20;
+
 struct gemm_plan {
   int device = 0;
   int64_t M = 0, N = 0, K = 0;
@@ -138,6 +144,18 @@ struct gemm_plan {
   void* hA = nullptr;
   void* hB = nullptr;
   void* hC = nullptr;
+  // gemm_run_host pipelining (see gemm_run_host): row panels of A and C, run
+  // by panel plans of their own; copies in on two streams, out on a third.
+  gemm_tuning_t tuning{};
+  bool has_tuning = false;
+  int64_t panel_rows = 0;          // 0: no row panels yet chosen
+  int num_panels = 0;
+  gemm_plan* panel_full = nullptr;  // plan for panel_rows rows
+  gemm_plan* panel_last = nullptr;  // plan for a shorter last panel, if any
+  cudaStream_t copy_in[2] = {nullptr, nullptr};
+  cudaStream_t copy_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_b[2] = {nullptr, nullptr}, ev_done = nullptr;
+  cudaEvent_t ev_a[kHostPanelsMax] = {}, ev_c[kHostPanelsMax] = {};
 
   int last_pads = 0;
   int last_tma_store = 0;
@@ -550,6 +568,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     delete p;
     return cuda_fail(e, "cudaMemset(status)");
   }
+  if (tuning) {
+    p->tuning = *tuning;
+    p->has_tuning = true;
+  }
   *out = p;
   return GEMM_OK;
 }
@@ -779,6 +801,47 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   return GEMM_OK;
 }
 
+// Row panels for gemm_run_host: plans of panel_rows rows (and a shorter last
+// panel), plus the copy streams and events, made on first use.
+static gemm_status_t host_panels_setup(gemm_plan_t* plan) {
+  if (plan->panel_rows > 0) return GEMM_OK;
+  const int64_t M = plan->M;
+  int panels = static_cast<int>(std::min<int64_t>(kHostPanelsMax, M / kHostPanelMinRows));
+  const int64_t tile_m = static_cast<int64_t>(kBM) * plan->cg;
+  if (panels < 2) {
+    plan->panel_rows = M;
+    plan->num_panels = 1;
+    return GEMM_OK;
+  }
+  const int64_t rows = cdiv(cdiv(M, panels), tile_m) * tile_m;  // whole tiles per panel
+  panels = static_cast<int>(cdiv(M, rows));
+  const gemm_tuning_t* t = plan->has_tuning ? &plan->tuning : nullptr;
+  gemm_status_t st = gemm_plan_create_ex(&plan->panel_full, rows, plan->N, plan->K, plan->dtype,
+                                         plan->epi, plan->stages, plan->variant, plan->device, t);
+  if (st != GEMM_OK) return st;
+  const int64_t last = M - (panels - 1) * rows;
+  if (last != rows) {
+    st = gemm_plan_create_ex(&plan->panel_last, last, plan->N, plan->K, plan->dtype, plan->epi,
+                             plan->stages, plan->variant, plan->device, t);
+    if (st != GEMM_OK) return st;
+  }
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+    e = cudaStreamCreateWithFlags(&plan->copy_in[i], cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->copy_out, cudaStreamNonBlocking);
+  cudaEvent_t* evs[] = {&plan->ev_start, &plan->ev_b[0], &plan->ev_b[1], &plan->ev_done};
+  for (cudaEvent_t* ev : evs)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  for (int i = 0; i < panels && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&plan->ev_a[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->ev_c[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "streams/events for gemm_run_host");
+  plan->panel_rows = rows;
+  plan->num_panels = panels;
+  return GEMM_OK;
+}
+
 gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, void* hC,
                             int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                             gemm_epilogue_t epi, int stages, void* stream_handle) {
@@ -789,8 +852,9 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
   if (M != plan->M || N != plan->N || K != plan->K || dtype != plan->dtype || epi != plan->epi ||
       stages != plan->stages)
     return fail(GEMM_ERR_PLAN_MISMATCH, "run arguments differ from the plan");
+  const size_t esC = plan->out_f32 ? 4 : 2;
   const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
-  const size_t bytesC = static_cast<size_t>(M) * N * (plan->out_f32 ? 4 : 2);
+  const size_t bytesC = static_cast<size_t>(M) * N * esC;
   if (bytesC == 0) return GEMM_OK;
   if (!hC || (bytesA && !hA) || (bytesB && !hB))
     return fail(GEMM_ERR_INVALID_ARG, "NULL host buffer");
@@ -803,15 +867,85 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
     if (bytesB && (e = cudaMalloc(&plan->hB, bytesB)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(B)");
     if ((e = cudaMalloc(&plan->hC, bytesC)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(C)");
   }
-  if (bytesA && (e = cudaMemcpyAsync(plan->hA, hA, bytesA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-    return cuda_fail(e, "copy A to device");
-  if (bytesB && (e = cudaMemcpyAsync(plan->hB, hB, bytesB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-    return cuda_fail(e, "copy B to device");
-  st = gemm_run(plan, plan->hA, plan->hB, plan->hC, M, N, K, dtype, epi, stages, stream_handle);
-  if (st != GEMM_OK) return st;
-  if ((e = cudaMemcpyAsync(hC, plan->hC, bytesC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-    return cuda_fail(e, "copy C to host");
-  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  const bool pipelined = K > 0 && bytesA + bytesB + bytesC >= kHostPanelMinBytes;
+  if (pipelined) {
+    st = host_panels_setup(plan);
+    if (st != GEMM_OK) return st;
+  }
+  if (!pipelined || plan->num_panels < 2) {
+    if (bytesA && (e = cudaMemcpyAsync(plan->hA, hA, bytesA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      return cuda_fail(e, "copy A to device");
+    if (bytesB && (e = cudaMemcpyAsync(plan->hB, hB, bytesB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      return cuda_fail(e, "copy B to device");
+    st = gemm_run(plan, plan->hA, plan->hB, plan->hC, M, N, K, dtype, epi, stages, stream_handle);
+    if (st != GEMM_OK) return st;
+    if ((e = cudaMemcpyAsync(hC, plan->hC, bytesC, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+      return cuda_fail(e, "copy C to host");
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return GEMM_OK;
+  }
+
+  // Pipelined: B (needed by every panel) comes in first, its two halves on two
+  // copy streams; then the row panels of A, alternating between them.  Panel
+  // i's GEMM runs on the caller's stream once its A rows (and B) are in, and
+  // its C rows go back on a third stream while the next panel computes.
+  const int P = plan->num_panels;
+  const int64_t R = plan->panel_rows;
+  auto ck = [&](cudaError_t err, const char* what) -> bool {
+    if (err != cudaSuccess) {
+      cuda_fail(err, what);
+      return false;
+    }
+    return true;
+  };
+  const char* hAb = static_cast<const char*>(hA);
+  const char* hBb = static_cast<const char*>(hB);
+  char* hCb = static_cast<char*>(hC);
+  char* dA = static_cast<char*>(plan->hA);
+  char* dB = static_cast<char*>(plan->hB);
+  char* dC = static_cast<char*>(plan->hC);
+  if (!ck(cudaEventRecord(plan->ev_start, stream), "record start")) return GEMM_ERR_CUDA;
+  const size_t halfB = (bytesB / 2) & ~static_cast<size_t>(15);
+  for (int s = 0; s < 2; ++s) {
+    if (!ck(cudaStreamWaitEvent(plan->copy_in[s], plan->ev_start, 0), "copy stream wait")) return GEMM_ERR_CUDA;
+    const size_t off = s == 0 ? 0 : halfB, len = s == 0 ? halfB : bytesB - halfB;
+    if (len && !ck(cudaMemcpyAsync(dB + off, hBb + off, len, cudaMemcpyHostToDevice, plan->copy_in[s]),
+                   "copy B to device"))
+      return GEMM_ERR_CUDA;
+    if (!ck(cudaEventRecord(plan->ev_b[s], plan->copy_in[s]), "record B")) return GEMM_ERR_CUDA;
+  }
+  for (int i = 0; i < P; ++i) {
+    const int64_t rows = std::min<int64_t>(R, M - i * R);
+    const size_t a_off = static_cast<size_t>(i) * R * K * 2, a_len = static_cast<size_t>(rows) * K * 2;
+    cudaStream_t cs = plan->copy_in[i & 1];
+    if (!ck(cudaMemcpyAsync(dA + a_off, hAb + a_off, a_len, cudaMemcpyHostToDevice, cs), "copy A panel"))
+      return GEMM_ERR_CUDA;
+    if (!ck(cudaEventRecord(plan->ev_a[i], cs), "record A panel")) return GEMM_ERR_CUDA;
+  }
+  if (!ck(cudaStreamWaitEvent(stream, plan->ev_b[0], 0), "wait B") ||
+      !ck(cudaStreamWaitEvent(stream, plan->ev_b[1], 0), "wait B"))
+    return GEMM_ERR_CUDA;
+  if (!ck(cudaStreamWaitEvent(plan->copy_out, plan->ev_start, 0), "copy-out wait")) return GEMM_ERR_CUDA;
+  for (int i = 0; i < P; ++i) {
+    const int64_t rows = std::min<int64_t>(R, M - i * R);
+    gemm_plan* pp = rows == R ? plan->panel_full : plan->panel_last;
+    if (!ck(cudaStreamWaitEvent(stream, plan->ev_a[i], 0), "wait A panel")) return GEMM_ERR_CUDA;
+    st = gemm_run(pp, dA + static_cast<size_t>(i) * R * K * 2, dB,
+                  dC + static_cast<size_t>(i) * R * N * esC, rows, N, K, dtype, epi, stages,
+                  stream_handle);
+    if (st != GEMM_OK) return st;
+    if (!ck(cudaEventRecord(plan->ev_c[i], stream), "record C panel") ||
+        !ck(cudaStreamWaitEvent(plan->copy_out, plan->ev_c[i], 0), "copy-out wait"))
+      return GEMM_ERR_CUDA;
+    const size_t c_off = static_cast<size_t>(i) * R * N * esC, c_len = static_cast<size_t>(rows) * N * esC;
+    if (!ck(cudaMemcpyAsync(hCb + c_off, dC + c_off, c_len, cudaMemcpyDeviceToHost, plan->copy_out),
+            "copy C panel to host"))
+      return GEMM_ERR_CUDA;
+  }
+  if (!ck(cudaEventRecord(plan->ev_done, plan->copy_out), "record done") ||
+      !ck(cudaStreamWaitEvent(stream, plan->ev_done, 0), "wait done") ||
+      !ck(cudaStreamSynchronize(stream), "cudaStreamSynchronize"))
+    return GEMM_ERR_CUDA;
   return GEMM_OK;
 }
 
@@ -835,6 +969,18 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
   }
   *device_status = h[0];
   if (detail) *detail = h[1];
+  // Panel plans of gemm_run_host keep status words of their own.
+  gemm_plan* panels[2] = {plan->panel_full, plan->panel_last};
+  for (gemm_plan* pp : panels) {
+    if (!pp) continue;
+    int32_t ds = 0, dd = 0;
+    gemm_status_t st = gemm_plan_check(pp, &ds, &dd);
+    if (st != GEMM_OK) return st;
+    if (*device_status == 0 && ds != 0) {
+      *device_status = ds;
+      if (detail) *detail = dd;
+    }
+  }
   return GEMM_OK;
 }
 
@@ -861,6 +1007,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->out_f32 = plan->out_f32;
   info->b_kn = plan->b_kn;
   info->k_sub = plan->k_sub;
+  info->host_panels = plan->num_panels >= 2 ? plan->num_panels : 0;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
   return GEMM_OK;
 }
@@ -878,8 +1025,18 @@ void gemm_plan_destroy(gemm_plan_t* plan) {
       if (plan->hA) cudaFree(plan->hA);
       if (plan->hB) cudaFree(plan->hB);
       if (plan->hC) cudaFree(plan->hC);
+      for (cudaStream_t cs : {plan->copy_in[0], plan->copy_in[1], plan->copy_out})
+        if (cs) cudaStreamDestroy(cs);
+      for (cudaEvent_t ev : {plan->ev_start, plan->ev_b[0], plan->ev_b[1], plan->ev_done})
+        if (ev) cudaEventDestroy(ev);
+      for (int i = 0; i < kHostPanelsMax; ++i) {
+        if (plan->ev_a[i]) cudaEventDestroy(plan->ev_a[i]);
+        if (plan->ev_c[i]) cudaEventDestroy(plan->ev_c[i]);
+      }
     }
   }
+  gemm_plan_destroy(plan->panel_full);
+  gemm_plan_destroy(plan->panel_last);
   delete plan;
 }
 

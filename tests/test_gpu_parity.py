@@ -257,6 +257,42 @@ def test_run_host_end_to_end():
     plan.close()
 
 
+@pytest.mark.parametrize("shape,tuning", [
+    ((4096, 2048, 2048), {}),                          # 4 panels of 1024 rows
+    ((3000, 3072, 2000), {}),                          # 2 panels, shorter last one
+    ((2304, 4096, 2050), {"b_kn": 1}),                 # K x N B, padded K
+    ((2048, 3072, 1024), {"out_f32": 1, "cta_group": 1}),
+])
+def test_run_host_row_panels(shape, tuning):
+    # Problems with >= 32 MiB of copies run as row panels: B first on two copy
+    # streams, A panels alternating, each panel's GEMM as soon as its rows are
+    # in, C panels copied back on a third stream.  Checked at sampled positions
+    # (every panel's first and last rows included), twice on the same plan.
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M, N, K = shape
+    A, B = gemm_inputs.custom(M, N, K, seed=M + N + K)
+    f32 = tuning.get("out_f32", 0) == 1
+    Bh = (B.t().contiguous() if tuning.get("b_kn") else B).pin_memory()
+    C = torch.empty(M, N, dtype=torch.float32 if f32 else torch.float16).pin_memory()
+    plan = sg.Plan(M, N, K, "f16", stages=6, **tuning)
+    stream = torch.cuda.current_stream()
+    rows = [0, M - 1] + [r for i in range(1, 8) for r in (i * M // 8 - 1, i * M // 8)]
+    r = np.array(rows * 40, dtype=np.int64)
+    c = np.random.default_rng(M).integers(0, N, len(r)).astype(np.int64)
+    ref = oracle.gemm_nt_entries(A, B, "f16", r, c)
+    for _ in range(2):
+        C.fill_(float("nan"))
+        plan.run_host(A.pin_memory().data_ptr(), Bh.data_ptr(), C.data_ptr(), stream.cuda_stream)
+        assert plan.check()[0] == 0
+        assert torch.isfinite(C).all()
+        got = C.numpy()[r, c].astype(np.float64) if f32 else \
+            oracle.decode(gu.bits(C)[r, c], "f16")
+        st = tolerance.compare(got, ref, "f32" if f32 else "f16")
+        assert st["ok"], st
+    assert plan.info()["host_panels"] >= 2
+    plan.close()
+
+
 def test_matmul_nt_torch_layer_on_current_stream():
     import software_pipelined_tiled_gemm_gb300 as sg
     A, B = gemm_inputs.custom(256, 512, 320, dtype="bf16", seed=22)
