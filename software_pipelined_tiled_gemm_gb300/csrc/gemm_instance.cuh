@@ -1,8 +1,8 @@
 // gemm_instance.cuh -- defines the launchers of one kernel shape.  Each shape
 // has four instances -- with or without the narrow-tile / stream-K code
-// (kSplit), for B stored N x K or K x N (kKN) -- and four more: for single-CTA
-// shapes with B's copies marked evict-first (kStream), for CTA pairs with two
-// K slices per ring slot (kSub).  The launcher picks the one the plan's
+// (kSplit), for B stored N x K or K x N (kKN) -- and more: for single-CTA
+// shapes, with B's copies marked evict-first (kStream), with one or two K
+// slices per ring slot (kSub); for CTA pairs, with two K slices per slot.  The launcher picks the one the plan's
 // parameters need, so no instance carries a runtime branch on these choices
 // in its copy and MMA loops.
 #pragma once
@@ -32,6 +32,7 @@ cudaError_t set_smem_all(size_t smem) {
   cudaError_t e = set_smem_layouts<BN, CG, false, 1>(smem);
   if constexpr (CG == 1) {
     if (e == cudaSuccess) e = set_smem_layouts<BN, CG, true, 1>(smem);
+    if (e == cudaSuccess) e = set_smem_layouts<BN, CG, true, 2>(smem);
   } else {
     if (e == cudaSuccess) e = set_smem_layouts<BN, CG, false, 2>(smem);
   }
@@ -59,12 +60,14 @@ cudaError_t launch_layout(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
 
 // Picks the instance for the plan: narrow / stream-K code or not, B layout,
 // evict-first B copies (single CTAs only) and two K slices per ring slot
-// (CTA pairs only).
+// (CTA pairs, and single CTAs streaming B).
 template <int BN, int CG>
 cudaError_t launch_instance(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
                             const CUtensorMap& b, const CUtensorMap& bt, const CUtensorMap& c,
                             const CUtensorMap& bp, const Params& p) {
   if constexpr (CG == 1) {
+    if (p.b_stream && p.k_sub == 2)
+      return launch_layout<BN, CG, true, 2>(cfg, a, b, bt, c, bp, p);
     if (p.b_stream) return launch_layout<BN, CG, true, 1>(cfg, a, b, bt, c, bp, p);
   } else {
     if (p.k_sub == 2) return launch_layout<BN, CG, false, 2>(cfg, a, b, bt, c, bp, p);

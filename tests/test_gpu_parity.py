@@ -555,6 +555,9 @@ def test_few_tiles_split_k_in_two_bit_exact(shape):
     plan = sg.Plan(M, N, K, "f16", stages=6)
     info = plan.info()
     assert info["stream_k"] == 1 and info["grid"] == 2 * info["num_tiles"], info
+    # one row of single-CTA tiles streams B: two K slices per ring slot (with
+    # K = 1100, 9 slots per tile, so the halves meet inside a slot's range)
+    assert info["k_sub"] == (2 if M <= 128 else 1), info
     a, b = A.cuda(), B.cuda()
     for _ in range(2):
         c = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
