@@ -466,12 +466,13 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   // most a quarter full.
   const int64_t k_blocks = cdiv(K, kBK);
   // CTA pairs, and single CTAs streaming B (one row of tiles), with an even
-  // ring of >= 4 slices group the slices in pairs: stages / 2 slots of two K
+  // ring of >= 6 slices group the slices in pairs: stages / 2 slots of two K
   // slices each, the same shared memory, but one barrier round trip per 8
   // MMAs instead of 4 (measured +2-5 % on pairs) and each B row read in
-  // 256-byte runs (+8-21 % on 64-128-row problems).
+  // 256-byte runs (+8-21 % on 64-128-row problems).  Two slots (4 slices)
+  // are too shallow: 8192^3 drops from 1647 to 1498 TFLOP/s.
   p->k_sub = ((chosen_cg == 2 || p->tiles_m == 1) && variant == GEMM_PIPELINED &&
-              stages % 2 == 0 && stages >= 4 && k_blocks >= 4)
+              stages % 2 == 0 && stages >= 6 && k_blocks >= 4)
                  ? 2
                  : 1;
   const int64_t k_slots = cdiv(K, kBK * p->k_sub);

@@ -71,8 +71,8 @@ def test_cta_pair_every_ring_depth_bit_exact(stages):
     C, info, canary = gu.run_device(A, B, "f16", stages=stages, cta_group=2, tile_n=tile_n,
                                     max_ctas=4)
     assert canary and info["cta_group"] == 2 and info["grid"] == 4
-    # even rings of >= 4 slices run as stages / 2 slots of two K slices
-    assert info["k_sub"] == (2 if stages % 2 == 0 and stages >= 4 else 1)
+    # even rings of >= 6 slices run as stages / 2 slots of two K slices
+    assert info["k_sub"] == (2 if stages % 2 == 0 and stages >= 6 else 1)
     _assert_bit_exact(A, B, "f16", C)
 
 
