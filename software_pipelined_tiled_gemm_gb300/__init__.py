@@ -14,7 +14,9 @@ call raises.
 Convenience layer: :func:`matmul_nt` takes torch CUDA tensors A (M,K) and
 B (N,K), caches a plan per problem, and launches on the current stream --
 the operation of the TileLang tutorial's ``matmul_auto`` (A (M,K), B (N,K),
-``T.gemm(..., transpose_B=True)``) with an optional tanh-GELU epilogue.
+``T.gemm(..., transpose_B=True)``) with an optional tanh-GELU or ReLU
+epilogue and fp16/bf16 or fp32 output.  :func:`matmul_nn` takes B as (K,N),
+the form of the Mosaic GPU guide's matmul example.
 """
 from __future__ import annotations
 
@@ -327,7 +329,9 @@ def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", 
     A: (M, K) and B: (N, K) CUDA tensors of the same dtype (float16 or
     bfloat16), contiguous.  epilogue: None, "gelu" or "relu".  Returns C
     (M, N) of that dtype, or of float32 when out_dtype is torch.float32
-    (``out`` if given).
+    (``out`` if given).  ``tuning`` keywords go to :class:`Plan` (tile_n,
+    cta_group, raster_group, max_ctas, tail_split, timeout_ns); plans are
+    cached per shape, dtype, epilogue and tuning.
     """
     import torch
     b_kn = bool(tuning.pop("_b_kn", False))

@@ -55,14 +55,43 @@ KERNEL_FILES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "gemm_instance.
                 "gemm_pair256.cu"]
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with comments removed and each line stripped of
+    surrounding whitespace (blank lines dropped); string and character
+    literals are kept as they are."""
+    out = []
+    i, n = 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.strip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_digest() -> str:
-    """Content hash of the GEMM kernel's device code only (what an ncu capture
-    of the kernel depends on), independent of the host planner."""
+    """Hash of the GEMM kernel's device code only (what an ncu capture of the
+    kernel depends on): comments and layout do not count, and the host planner
+    is left out."""
     h = hashlib.sha256()
     for f in KERNEL_FILES:
         h.update(f.encode())
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + FLAGS).encode())
     return h.hexdigest()[:16]
 

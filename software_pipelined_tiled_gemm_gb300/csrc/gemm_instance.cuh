@@ -1,10 +1,10 @@
 // gemm_instance.cuh -- defines the launchers of one kernel shape.  Each shape
 // has four instances -- with or without the narrow-tile / stream-K code
 // (kSplit), for B stored N x K or K x N (kKN) -- and more: for single-CTA
-// shapes, with B's copies marked evict-first (kStream), with one or two K
-// slices per ring slot (kSub); for CTA pairs, with two K slices per slot.  The launcher picks the one the plan's
-// parameters need, so no instance carries a runtime branch on these choices
-// in its copy and MMA loops.
+// shapes, with B's copies marked evict-first (kStream) and one or two K
+// slices per ring slot (kSub); for CTA pairs, with two K slices per slot.
+// The launcher picks the one the plan's parameters need, so no instance
+// carries a runtime branch on these choices in its copy and MMA loops.
 #pragma once
 
 #include "gemm_kernel.cuh"

@@ -1,38 +1,46 @@
 // gemm_kernel.cuh -- persistent, warp-specialised sm_103a GEMM
 //
-//   C[M,N] = epi(A[M,K] . B[N,K]^T), fp16/bf16 in, fp32 accumulate in TMEM.
+//   C[M,N] = epi(A[M,K] . B^T), B stored N x K (or K x N), fp16/bf16 in,
+//   fp32 accumulate in TMEM, fp16/bf16 (or fp32) out, epi in {none, tanh-GELU,
+//   ReLU}.
 //
 // Structure (TileLang tutorial ch. 11 "pipelined_gemm.py", matmul_auto, for
 // the tile loop; Mosaic GPU pipelining guide, "Warp Specialization", for the
 // split into a memory thread and compute threads):
 //
-//   warp 0  (one lane)  TMA producer: for every tile the CTA owns and every
-//                       64-wide K slice, wait until ring slot s is empty,
-//                       then load the A tile (128 x 64) and B tile (BN x 64)
-//                       into slot s with 128-byte swizzling; the copy engine
-//                       counts the bytes onto full[s].
-//   warp 1  (one lane)  MMA issuer: wait full[s], issue four
-//                       tcgen05.mma (K = 16 each) into the tile's TMEM
-//                       accumulator, then tcgen05.commit -> empty[s].  The
-//                       slot is released only when those MMAs have finished
-//                       reading it (the hazard the guide's delay_release
-//                       covers), and the issuer never waits on its own MMAs.
-//                       After the last K slice: commit -> tmem_full[acc].
-//   warps 2-5           epilogue: wait tmem_full[acc], tcgen05.ld 32 rows x
-//                       64 columns per step, optional tanh-GELU in fp32,
-//                       round to fp16/bf16, write a swizzled staging tile and
-//                       send it out with a TMA store (or masked st.global
-//                       when C's pitch is not 16-byte aligned); then arrive
-//                       on tmem_empty[acc].
+//   warp 0  (one lane)  TMA producer: for every unit of work and every ring
+//                       slot's worth of K (one or two 64-wide slices), wait
+//                       until slot s is empty, then copy the A rows and B
+//                       rows of those slices into slot s with 128-byte
+//                       swizzling; the copy engine counts the bytes onto
+//                       full[s].
+//   warp 1  (one lane)  MMA issuer: wait full[s], issue 4 tcgen05.mma per
+//                       slice (K = 16 each) into the unit's TMEM accumulator,
+//                       then tcgen05.commit -> empty[s].  The slot is
+//                       released only when those MMAs have finished reading
+//                       it (the hazard the guide's delay_release covers), and
+//                       the issuer never waits on its own MMAs.  After the
+//                       unit's last slot: commit -> tmem_full[acc].
+//   warps 2-5           epilogue: wait tmem_full[acc]; for stream-K owners,
+//                       add the other walker's fp32 partial; then tcgen05.ld
+//                       32 rows x 64 columns per step, apply the epilogue
+//                       function, round, write a swizzled staging tile and
+//                       send it out with a TMA store (or row-wise stores when
+//                       C's pitch is not 16-byte aligned); then arrive on
+//                       tmem_empty[acc].
 //
-// With two TMEM accumulators the epilogue of tile t overlaps the main loop
-// of tile t+1.  The CTAs are persistent: CTA b walks tiles b, b + grid, ...
-// of a grouped ("rasterised") tile order that keeps `raster_group` tile rows
-// together so concurrently running CTAs share A and B slices in L2.
+// With two TMEM accumulators the epilogue of one unit overlaps the main loop
+// of the next.  CTA pairs (cluster of 2, tcgen05.mma.cta_group::2) compute
+// 256-row tiles: each CTA copies its own 128 rows of A and half of B's rows,
+// and the even CTA issues the MMAs for both.  The CTAs (or pairs) are
+// persistent walkers over a grouped ("rasterised") tile order that keeps
+// `raster_group` tile rows together, so concurrently running walkers share A
+// and B rows in L2; the last, partial wave is shared out stream-K (or cut
+// into narrow tiles).
 //
-// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
-// records GEMM_ERR_TIMEOUT in the status word and its role stops, after which
-// the CTA drains its in-flight copies and MMAs and frees its TMEM.
+// Every wait is bounded by a wall-clock limit; a wait that runs out records
+// GEMM_ERR_TIMEOUT in the status word and its role stops, after which the CTA
+// drains its in-flight copies and MMAs and frees its TMEM.
 #pragma once
 
 #include <cuda.h>
@@ -201,6 +209,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Epilogue function EPI on 32 fp32 accumulator values held as raw words:
+// 1 tanh-GELU, 2 ReLU (max(x, 0), with -0 and NaN giving +0).  Callers pick
+// EPI once per 64-column chunk, so the unrolled loop holds no per-element
+// branch (a per-element switch cost 11-12 % at 4096^3).
 template <int EPI>
 __device__ __forceinline__ void apply_epilogue32(uint32_t (&r)[32]) {
 #pragma unroll
