@@ -230,10 +230,22 @@ def cpu_baseline(A, B, w, seconds, threads=0, epi=None):
     oracle.gemm_nt(A[:rows], B, w.dtype, epilogue=epi, threads=threads)
     el = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
-    return {"value": flops / el / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": "%d of %d output rows (all %d columns, full K=%d), %.1f s" % (
-                rows, w.M, w.N, w.K, el)}, rows
+    cores = oracle.max_threads()
+    out = {"value": flops / el / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": "%d of %d output rows (all %d columns, full K=%d), %.1f s" % (
+               rows, w.M, w.N, w.K, el)}
+    # The same oracle on one core, on a smaller block (about seconds / 5).
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A[:1], B, w.dtype, epilogue=epi, threads=1)
+    dt1 = max(time.perf_counter() - t0, 1e-3)
+    rows1 = int(max(1, min(w.M, seconds / 5 / dt1)))
+    t0 = time.perf_counter()
+    oracle.gemm_nt(A[:rows1], B, w.dtype, epilogue=epi, threads=1)
+    el1 = time.perf_counter() - t0
+    oracle.gemm_nt(A[:1], B, w.dtype, epilogue=epi, threads=cores)  # restore the thread count
+    out["single_thread"] = {"value": 2.0 * rows1 * w.N * w.K / el1 / 1e12, "unit": UNIT,
+                            "sample": "%d output rows, %.1f s" % (rows1, el1)}
+    return out, rows
 
 
 def run_reference(args, w, ws, rank):
@@ -452,8 +464,11 @@ def main():
     peak = float(peaks.get(peak_key, FALLBACK_TFLOPS))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM))
     digest = source_digest()
-    variant_key = w.name + ("" if not nn else ":nn") + ("" if epi_name == w.epilogue else
-                                                         ":" + epi_name)
+    # Profile key: the workload plus whatever changes the kernel or its traffic.
+    variant_key = (w.name + ("" if not nn else ":nn")
+                   + ("" if epi_name == w.epilogue else ":" + epi_name)
+                   + (":single" if args.variant == "single_buffer" else "")
+                   + (":f32" if args.out_f32 else ""))
     traffic = traffic_from_profiles(variant_key, digest)
     min_bytes = 2.0 * (w.M * w.K + w.N * w.K) + float(w.M * w.N * C.element_size())
     # Below the ridge point (peak flops / HBM bandwidth) the GEMM is bound by
