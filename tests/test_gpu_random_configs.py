@@ -1,0 +1,128 @@
+"""Randomised GPU parity: seeded draws over shapes and plan options.
+
+Each case draws M, N, K (1 .. ~700), the dtype, the epilogue, the B layout,
+the CTA group, the ring depth, the last-wave scheme, fp32 output and
+unaligned operand bases, runs the CUDA path through the C ABI and compares
+every element with the fp64 oracle (2 ulp + 1e-3 per element, relative
+Frobenius 1e-3).  Option combinations the planner rejects by design (for
+example narrow tail tiles with a K x N B, or a ring that does not fit shared
+memory) raise GemmError and are counted as skipped; most draws must run.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import gemm_inputs
+import oracle
+from tests import gpu_util as gu
+from tests import tolerance
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import software_pipelined_tiled_gemm_gb300 as sg
+    sg.load_library()
+
+
+def _draw(rng):
+    def dim():
+        # mostly ragged sizes, sometimes tile multiples or tiny ones
+        kind = rng.integers(0, 4)
+        if kind == 0:
+            return int(rng.integers(1, 33))
+        if kind == 1:
+            return int(rng.integers(1, 6)) * 128
+        return int(rng.integers(33, 700))
+    return {
+        "M": dim(), "N": dim(), "K": dim(),
+        "dtype": str(rng.choice(["f16", "bf16"])),
+        "epilogue": [None, "gelu", "relu"][int(rng.integers(0, 3))],
+        "b_kn": int(rng.integers(0, 2)),
+        "cta_group": int(rng.choice([0, 1, 2])),
+        "stages": int(rng.choice([1, 2, 3, 4, 5, 6])),
+        "tail_split": int(rng.choice([0, 0, -1, 1, 2])),
+        "out_f32": int(rng.integers(0, 4) == 0),
+        "max_ctas": int(rng.choice([0, 0, 3, 7])),
+        "offsets": tuple(int(x) for x in rng.choice([0, 0, 0, 1, 3, 8], size=3)),
+    }
+
+
+def _run_case(cfg):
+    import software_pipelined_tiled_gemm_gb300 as sg
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    dtype, epi = cfg["dtype"], cfg["epilogue"]
+    A, B = gemm_inputs.custom(M, N, K, dtype=dtype, dist="normal_scaled",
+                              seed=M * 7919 + N * 31 + K)
+    tuning = {k: cfg[k] for k in ("b_kn", "cta_group", "tail_split", "out_f32", "max_ctas")}
+    if tuning["cta_group"] == 2:
+        tuning["tile_n"] = 256 if cfg["stages"] <= 6 else 128
+    dev = torch.device("cuda", 0)
+    td = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    ctd = torch.float32 if cfg["out_f32"] else td
+    a_off, b_off, c_off = cfg["offsets"]
+    if cfg["out_f32"]:
+        c_off = c_off // 2 * 2  # fp32 C must stay 4-byte aligned
+
+    def place(x, off, dt):
+        buf = torch.zeros(x.numel() + off + 64, dtype=dt, device=dev)
+        view = buf[off:off + x.numel()]
+        view.copy_(x.reshape(-1).to(dev))
+        return buf, view
+
+    Bd = B.t().contiguous() if cfg["b_kn"] else B
+    _, a = place(A, a_off, td)
+    _, b = place(Bd, b_off, td)
+    cbuf = torch.full((M * N + c_off + 64,), float("nan"), dtype=ctd, device=dev)
+    c = cbuf[c_off:c_off + M * N]
+    plan = sg.Plan(M, N, K, dtype, epi, cfg["stages"],
+                   "single_buffer" if cfg["stages"] == 1 else "pipelined", 0, **tuning)
+    try:
+        plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                     torch.cuda.current_stream(dev).cuda_stream)
+        torch.cuda.synchronize(dev)
+        ds, detail = plan.check()
+        assert ds == 0, "device status %d detail %#x" % (ds, detail)
+        info = plan.info()
+    finally:
+        plan.close()
+    ref = oracle.gemm_nt(A, B, dtype, epilogue=epi)
+    if cfg["out_f32"]:
+        got = c.view(M, N).cpu().double().numpy()
+        st = tolerance.compare(got, ref, "f32")
+    else:
+        got = oracle.decode(gu.bits(c.view(M, N).cpu()), dtype)
+        st = tolerance.compare(got, ref, dtype)
+    # nothing written outside C
+    around = torch.cat([cbuf[:c_off], cbuf[c_off + M * N:]]).cpu()
+    assert torch.isnan(around.float()).all(), "write outside C"
+    return st, info
+
+
+@pytest.mark.parametrize("seed", [20261202, 7])
+def test_random_configurations_match_the_oracle(seed):
+    import software_pipelined_tiled_gemm_gb300 as sg
+    rng = np.random.default_rng(seed)
+    ran, skipped, failures = 0, 0, []
+    for i in range(N_CASES):
+        cfg = _draw(rng)
+        try:
+            st, info = _run_case(cfg)
+        except sg.GemmError as e:
+            if e.status in (sg.GEMM_ERR_INVALID_ARG, sg.GEMM_ERR_SMEM_BUDGET):
+                skipped += 1
+                continue
+            raise
+        ran += 1
+        if not st["ok"]:
+            failures.append((i, cfg, st, info))
+    print("seed %d: %d configurations ran, %d rejected by the planner" % (seed, ran, skipped))
+    assert not failures, failures[:3]
+    assert ran >= N_CASES * 2 // 3, (ran, skipped)
