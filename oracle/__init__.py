@@ -15,6 +15,8 @@ Definitions followed (see the C file for the full statement):
   * tanh-GELU as written in the Triton lecture notes ("GeLU") and the
     XLA:GPU emitters page (loop-emitter example, ``@gelu``), constant
     sqrt(2/pi) = 0.7978845608.
+  * Bias (no page defines one; the reading is a Linear layer's): one value
+    per output column, added to the exact sum before the epilogue.
 
 Every function here has a pin in ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
@@ -76,6 +78,13 @@ def _open(path):
     lib.oracle_gemm_nt_entries.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int,
                                            ctypes.c_int, i64p, i64p, i64, f64p, ctypes.c_int]
     lib.oracle_gemm_nt_entries.restype = ctypes.c_int
+    lib.oracle_gemm_nt_bias.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_int,
+                                        ctypes.c_int, f64p, ctypes.c_int]
+    lib.oracle_gemm_nt_bias.restype = ctypes.c_int
+    lib.oracle_gemm_nt_entries_bias.argtypes = [u16p, u16p, u16p, i64, i64, i64, ctypes.c_int,
+                                                ctypes.c_int, i64p, i64p, i64, f64p,
+                                                ctypes.c_int]
+    lib.oracle_gemm_nt_entries_bias.restype = ctypes.c_int
     lib.oracle_decode_array.argtypes = [u16p, i64, ctypes.c_int, f64p]
     lib.oracle_decode_array.restype = None
     lib.oracle_round_array.argtypes = [f64p, i64, ctypes.c_int, u16p]
@@ -149,37 +158,52 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-def gemm_nt(A, B, dtype, epilogue=None, threads: int = 0) -> np.ndarray:
-    """fp64 C[i,j] = epi(sum_k A[i,k] B[j,k]); A (M,K), B (N,K) bit patterns."""
+def _bias(bias, N):
+    """Bias bit patterns (N values) as a uint16 array and its pointer, or None."""
+    if bias is None:
+        return None, None
+    v = _u16(bias).reshape(-1)
+    if v.size != N:
+        raise ValueError("bias must have N = %d values" % N)
+    return v, _ptr(v, ctypes.c_uint16)
+
+
+def gemm_nt(A, B, dtype, epilogue=None, threads: int = 0, bias=None) -> np.ndarray:
+    """fp64 C[i,j] = epi(sum_k A[i,k] B[j,k] + bias[j]); A (M,K), B (N,K) and
+    bias (N values, optional) as bit patterns."""
     lib = _load()
     a, b = _u16(A), _u16(B)
     if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
         raise ValueError("A must be (M,K) and B (N,K)")
     M, K = a.shape
     N = b.shape[0]
+    bias_bits, bp = _bias(bias, N)  # keep the array alive across the call
     C = np.zeros((M, N), dtype=np.float64)
-    rc = lib.oracle_gemm_nt(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), M, N, K,
-                            _dt(dtype), _epi(epilogue), _ptr(C, ctypes.c_double), int(threads))
+    rc = lib.oracle_gemm_nt_bias(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), bp, M, N, K,
+                                 _dt(dtype), _epi(epilogue), _ptr(C, ctypes.c_double),
+                                 int(threads))
     if rc != 0:
         raise RuntimeError("oracle_gemm_nt failed")
     return C
 
 
-def gemm_nt_entries(A, B, dtype, rows, cols, epilogue=None, threads: int = 0) -> np.ndarray:
+def gemm_nt_entries(A, B, dtype, rows, cols, epilogue=None, threads: int = 0,
+                    bias=None) -> np.ndarray:
     """The same definition at chosen (row, col) positions only."""
     lib = _load()
     a, b = _u16(A), _u16(B)
     M, K = a.shape
     N = b.shape[0]
+    bias_bits, bp = _bias(bias, N)  # keep the array alive across the call
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     c = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
     if r.shape != c.shape:
         raise ValueError("rows and cols must have the same shape")
     out = np.zeros(r.shape, dtype=np.float64)
-    rc = lib.oracle_gemm_nt_entries(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), M, N, K,
-                                    _dt(dtype), _epi(epilogue),
-                                    _ptr(r, ctypes.c_int64), _ptr(c, ctypes.c_int64), r.size,
-                                    _ptr(out, ctypes.c_double), int(threads))
+    rc = lib.oracle_gemm_nt_entries_bias(_ptr(a, ctypes.c_uint16), _ptr(b, ctypes.c_uint16), bp,
+                                         M, N, K, _dt(dtype), _epi(epilogue),
+                                         _ptr(r, ctypes.c_int64), _ptr(c, ctypes.c_int64), r.size,
+                                         _ptr(out, ctypes.c_double), int(threads))
     if rc != 0:
         raise RuntimeError("oracle_gemm_nt_entries failed (index out of range?)")
     return out

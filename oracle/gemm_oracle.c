@@ -18,6 +18,10 @@
  *  - ReLU epilogue: max(x, 0), the accumulator clamp of the Triton lecture
  *    notes' matmul example (matmul_relu_kernel); zero and negative sums give
  *    +0.
+ *  - Bias: no page defines one.  Reading: a Linear layer's per-output-column
+ *    bias (the GELU workload is such a layer, Y = gelu(X . W^T)), one value
+ *    per column j in the input format, added to the exact sum before the
+ *    epilogue: C[i,j] = epi(sum_k A[i,k] B[j,k] + bias[j]).
  *  - Epilogue: the tanh-approximate GELU, 0.5 x (1 + tanh(sqrt(2/pi) (x +
  *    0.044715 x^3))), as the Triton lecture notes ("GeLU" example) and the
  *    XLA:GPU emitters page (loop-emitter example, function @gelu) write it;
@@ -157,12 +161,17 @@ static double* decode_matrix(const uint16_t* bits, int64_t count, int dtype) {
   return out;
 }
 
-/* C[i,j] = epi(sum_k A[i,k] * B[j,k]), all in fp64; epilogue 0 none,
- * 1 tanh-GELU, 2 ReLU.
+/* Bias of output column j: its exact value, or 0 without a bias vector. */
+static double bias_of(const uint16_t* bias, int64_t j, int dtype) {
+  return bias ? oracle_decode(bias[j], dtype) : 0.0;
+}
+
+/* C[i,j] = epi(sum_k A[i,k] * B[j,k] + bias[j]), all in fp64; epilogue 0
+ * none, 1 tanh-GELU, 2 ReLU; bias: N values in the input format, or NULL.
  * A: M x K row-major, B: N x K row-major, C: M x N row-major doubles.
  * Returns 0 on success, -1 on bad arguments or allocation failure. */
-int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
-                   int dtype, int epilogue, double* C, int threads) {
+int oracle_gemm_nt_bias(const uint16_t* A, const uint16_t* B, const uint16_t* bias, int64_t M,
+                        int64_t N, int64_t K, int dtype, int epilogue, double* C, int threads) {
   if (M < 0 || N < 0 || K < 0 || !C) return -1;
   if ((M > 0 && K > 0 && !A) || (N > 0 && K > 0 && !B)) return -1;
   set_threads(threads);
@@ -176,7 +185,7 @@ int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, i
       const double* b = Bd + j * K;
       double s = 0.0;
       for (int64_t k = 0; k < K; ++k) s += a[k] * b[k];
-      C[i * N + j] = apply_epilogue(s, epilogue);
+      C[i * N + j] = apply_epilogue(s + bias_of(bias, j, dtype), epilogue);
     }
   }
   free(Ad);
@@ -184,11 +193,17 @@ int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, i
   return 0;
 }
 
+int oracle_gemm_nt(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                   int dtype, int epilogue, double* C, int threads) {
+  return oracle_gemm_nt_bias(A, B, NULL, M, N, K, dtype, epilogue, C, threads);
+}
+
 /* Same definition, for `count` chosen entries (rows[t], cols[t]) only, so a
  * full-size product can be checked at sampled positions. */
-int oracle_gemm_nt_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
-                           int dtype, int epilogue, const int64_t* rows, const int64_t* cols,
-                           int64_t count, double* out, int threads) {
+int oracle_gemm_nt_entries_bias(const uint16_t* A, const uint16_t* B, const uint16_t* bias,
+                                int64_t M, int64_t N, int64_t K, int dtype, int epilogue,
+                                const int64_t* rows, const int64_t* cols, int64_t count,
+                                double* out, int threads) {
   if (M < 0 || N < 0 || K < 0 || count < 0 || (count > 0 && (!rows || !cols || !out))) return -1;
   for (int64_t t = 0; t < count; ++t)
     if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
@@ -199,9 +214,16 @@ int oracle_gemm_nt_entries(const uint16_t* A, const uint16_t* B, int64_t M, int6
     const uint16_t* b = B + cols[t] * K;
     double s = 0.0;
     for (int64_t k = 0; k < K; ++k) s += oracle_decode(a[k], dtype) * oracle_decode(b[k], dtype);
-    out[t] = apply_epilogue(s, epilogue);
+    out[t] = apply_epilogue(s + bias_of(bias, cols[t], dtype), epilogue);
   }
   return 0;
+}
+
+int oracle_gemm_nt_entries(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                           int dtype, int epilogue, const int64_t* rows, const int64_t* cols,
+                           int64_t count, double* out, int threads) {
+  return oracle_gemm_nt_entries_bias(A, B, NULL, M, N, K, dtype, epilogue, rows, cols, count, out,
+                                     threads);
 }
 
 /* Element-wise helpers over arrays, for the Python wrapper. */

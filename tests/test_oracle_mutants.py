@@ -36,6 +36,11 @@ MUTANTS = {
                              "if (epilogue == 9) return oracle_gelu_tanh(s);"),
     "relu_reflects": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : -x;"),
     "relu_leaky": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : 0.01 * x;"),
+    "bias_by_row": ("s + bias_of(bias, j, dtype)", "s + bias_of(bias, i, dtype)"),
+    "bias_after_epilogue": ("apply_epilogue(s + bias_of(bias, j, dtype), epilogue)",
+                            "apply_epilogue(s, epilogue) + bias_of(bias, j, dtype)"),
+    "bias_ignored": ("return bias ? oracle_decode(bias[j], dtype) : 0.0;", "return 0.0;"),
+    "bias_entries_by_row": ("s + bias_of(bias, cols[t], dtype)", "s + bias_of(bias, rows[t], dtype)"),
 }
 
 PIN_TESTS = [
@@ -58,6 +63,10 @@ PIN_TESTS = [
     lambda: pins.test_gemm_gelu_epilogue_applies_after_sum(),
     lambda: pins.test_relu_epilogue_on_a_transposed_identity(),
     lambda: pins.test_relu_epilogue_is_the_triton_clamp(),
+    lambda: pins.test_bias_alone_with_zero_a(),
+    lambda: pins.test_bias_is_exact_on_integers(),
+    lambda: pins.test_bias_is_added_before_the_epilogue(),
+    lambda: pins.test_bias_entries_equal_the_full_product(),
 ]
 
 

@@ -350,3 +350,63 @@ def test_relu_epilogue_is_the_triton_clamp():
     exact = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T
     assert np.array_equal(C, np.maximum(exact, 0).astype(np.float64))
     assert (exact < 0).any() and (exact > 0).any()
+
+
+# ------------------------------------------------------------------ bias --
+# No page defines a bias; the reading is a Linear layer's per-output-column
+# bias, added to the exact sum before the epilogue.
+
+def test_bias_alone_with_zero_a():
+    # A = 0 leaves C[i,j] = epi(bias[j]) in every row.  M < N so that a bias
+    # taken by row index instead of column index reads a different value.
+    M, N, K = 3, 7, 5
+    A = np.zeros((M, K), dtype=np.float16)
+    _, B = gemm_inputs.custom(1, N, K, seed=19)
+    bias = np.array([-2.5, -0.75, -0.0, 0.0, 0.5, 1.25, 3.0], dtype=np.float16)
+    b = bias.astype(np.float64)
+    for epi, f in ((None, lambda x: x), ("relu", lambda x: np.where(x > 0, x, 0.0)),
+                   ("gelu", lambda x: 0.5 * x * (1 + np.tanh(0.7978845608 * (x + 0.044715 * x ** 3))))):
+        C = oracle.gemm_nt(A, B, "f16", epilogue=epi, bias=bias)
+        assert np.allclose(C, np.broadcast_to(f(b), (M, N)), rtol=1e-15, atol=0), epi
+
+
+def test_bias_is_exact_on_integers():
+    # Integer A, B and bias: C = A B^T + bias exactly (numpy int64 arithmetic),
+    # for fp16 and bf16 patterns of the same integers.
+    for dtype, td in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        A, B = gemm_inputs.custom(9, 14, 32, dtype=dtype, dist="int", lo=-2, hi=2, seed=21)
+        bias_i = np.arange(-7, 7, dtype=np.int64) * 3
+        bias = torch.tensor(bias_i, dtype=td)
+        C = oracle.gemm_nt(A, B, dtype, bias=bias)
+        exact = A.to(torch.int64).numpy() @ B.to(torch.int64).numpy().T + bias_i[None, :]
+        assert np.array_equal(C, exact.astype(np.float64)), dtype
+
+
+def test_bias_is_added_before_the_epilogue():
+    # Sums that are negative but become positive with the bias: ReLU must see
+    # s + b (giving s + b), not s (giving b).
+    A = np.full((2, 4), 1.0, dtype=np.float16)
+    B = np.full((3, 4), -1.0, dtype=np.float16)          # every sum is -4
+    bias = np.array([5.0, 4.0, 6.5], dtype=np.float16)
+    C = oracle.gemm_nt(A, B, "f16", epilogue="relu", bias=bias)
+    assert np.array_equal(C, np.broadcast_to(np.array([1.0, 0.0, 2.5]), (2, 3)))
+    G = oracle.gemm_nt(A, B, "f16", epilogue="gelu", bias=bias)
+    x = np.array([1.0, 0.0, 2.5])
+    assert np.allclose(G[0], 0.5 * x * (1 + np.tanh(0.7978845608 * (x + 0.044715 * x ** 3))),
+                       rtol=1e-15, atol=0)
+
+
+def test_bias_entries_equal_the_full_product():
+    A, B = gemm_inputs.custom(11, 17, 40, seed=22)
+    bias = torch.linspace(-2, 2, 17).to(torch.float16)
+    C = oracle.gemm_nt(A, B, "f16", epilogue="gelu", bias=bias)
+    rows = np.array([0, 10, 5, 3], dtype=np.int64)
+    cols = np.array([16, 0, 8, 11], dtype=np.int64)
+    e = oracle.gemm_nt_entries(A, B, "f16", rows, cols, epilogue="gelu", bias=bias)
+    assert np.array_equal(e, C[rows, cols])
+
+
+def test_no_bias_is_a_zero_bias():
+    A, B = gemm_inputs.custom(5, 6, 16, seed=23)   # M < N (see test_bias_alone_with_zero_a)
+    z = torch.zeros(6, dtype=torch.float16)
+    assert np.array_equal(oracle.gemm_nt(A, B, "f16", bias=z), oracle.gemm_nt(A, B, "f16"))
