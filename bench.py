@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--epilogue", default="auto", choices=["auto", "none", "gelu", "relu"],
                     help="auto: the workload's own epilogue")
     ap.add_argument("--out-f32", action="store_true", help="write C in fp32")
+    ap.add_argument("--bias", action="store_true",
+                    help="add a seeded per-column bias before the epilogue (no e2e figure)")
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="auto: flush L2 between steps when the operands fit in it")
     ap.add_argument("--dist-reps", type=int, default=30,
@@ -329,13 +331,15 @@ def main():
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
     a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
+    bias_t = gemm_inputs.bias(w.N, w.dtype, seed=w.seed).to(dev) if args.bias else None
+    bias_p = bias_t.data_ptr() if bias_t is not None else 0
     operand_bytes = (w.M * w.K + w.N * w.K) * 2
     flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and operand_bytes <= L2_BYTES)
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            plan.run_ptr(a_p, b_p, c_p, sptr)
+            plan.run_ptr(a_p, b_p, c_p, sptr, bias_p)
     stream.synchronize()
     ds, detail = plan.check()
     if ds != 0:
@@ -358,7 +362,7 @@ def main():
     if not flush:
         ev0.record(stream)
         for _ in range(args.steps):
-            plan.run_ptr(a_p, b_p, c_p, sptr)
+            plan.run_ptr(a_p, b_p, c_p, sptr, bias_p)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         elapsed_ms = ev0.elapsed_time(ev1)
@@ -369,7 +373,7 @@ def main():
             for e0, e1 in evs:
                 scrub.fill_(1)
                 e0.record(stream)
-                plan.run_ptr(a_p, b_p, c_p, sptr)
+                plan.run_ptr(a_p, b_p, c_p, sptr, bias_p)
                 e1.record(stream)
         torch.cuda.synchronize(dev)
         elapsed_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -399,7 +403,7 @@ def main():
                 if flush:
                     scrub.fill_(1)
                 e0.record(stream)
-                plan.run_ptr(a_p, b_p, c_p, sptr)
+                plan.run_ptr(a_p, b_p, c_p, sptr, bias_p)
                 e1.record(stream)
         torch.cuda.synchronize(dev)
         t = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
@@ -411,18 +415,22 @@ def main():
     # Same protocol as the timed region: back to back between two events, or
     # (when flushing) each rep after an L2 flush, bracketed by its own events.
     cublas = None
+
+    def ref_mm():
+        return torch.matmul(A, bt) if bias_t is None else torch.addmm(bias_t, A, bt)
+
     if not args.no_cublas and epi is None and not args.out_f32:
         bt = B if nn else B.t()
         reps = 20
         with torch.cuda.stream(stream):
             for _ in range(3):
-                torch.matmul(A, bt)
+                ref_mm()
             if not flush:
                 c0 = torch.cuda.Event(enable_timing=True)
                 c1 = torch.cuda.Event(enable_timing=True)
                 c0.record(stream)
                 for _ in range(reps):
-                    torch.matmul(A, bt)
+                    ref_mm()
                 c1.record(stream)
             else:
                 cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -430,7 +438,7 @@ def main():
                 for e0, e1 in cevs:
                     scrub.fill_(1)
                     e0.record(stream)
-                    torch.matmul(A, bt)
+                    ref_mm()
                     e1.record(stream)
         torch.cuda.synchronize(dev)
         if not flush:
@@ -443,7 +451,7 @@ def main():
 
     # end-to-end through the C ABI with host buffers (pinned)
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not args.bias:
         hA, hB = A_cpu.pin_memory(), B_cpu.pin_memory()
         hC = torch.empty(w.M, w.N, dtype=c_dtype).pin_memory()
         eplan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, args.stages, args.variant, local, **tuning)
@@ -468,7 +476,8 @@ def main():
     variant_key = (w.name + ("" if not nn else ":nn")
                    + ("" if epi_name == w.epilogue else ":" + epi_name)
                    + (":single" if args.variant == "single_buffer" else "")
-                   + (":f32" if args.out_f32 else ""))
+                   + (":f32" if args.out_f32 else "")
+                   + (":bias" if args.bias else ""))
     traffic = traffic_from_profiles(variant_key, digest)
     min_bytes = 2.0 * (w.M * w.K + w.N * w.K) + float(w.M * w.N * C.element_size())
     # Below the ridge point (peak flops / HBM bandwidth) the GEMM is bound by
@@ -502,6 +511,7 @@ def main():
                 "workload": w.name, "M": w.M, "N": w.N, "K": w.K, "input_dtype": w.dtype,
                 "accumulate": "f32", "epilogue": epi_name, "variant": args.variant,
                 "layout": args.layout, "output_dtype": "f32" if args.out_f32 else w.dtype,
+                "bias": bool(args.bias),
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],

@@ -117,3 +117,22 @@ def custom(M: int, N: int, K: int, dtype: str = "f16", dist: str = "uniform", se
     """Draw (A, B) for an arbitrary shape with one of the recipes above."""
     w = Workload("custom", M, N, K, dtype, epilogue, dist, seed, lo=lo, hi=hi)
     return make(w)
+
+
+def bias(N: int, dtype: str = "f16", seed: int = 0, dist: str = "uniform", lo: float = -0.5,
+         hi: float = 0.5) -> torch.Tensor:
+    """A seeded per-column bias vector of N values, cast to fp16/bf16 with RNE.
+
+    dist "uniform": U[lo, hi] (default U[-0.5, 0.5], the scale of a Linear
+    layer's bias next to the GELU workload's pre-activations of std 1.28);
+    "int": integers U{lo..hi}, exact in both formats for the bit-exact tests.
+    The generator is seeded separately from the operands' (seed + 1000003).
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed + 1000003)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float16
+    if dist == "int":
+        v = torch.randint(int(lo), int(hi) + 1, (N,), generator=gen).to(torch.float32)
+    else:
+        v = torch.rand(N, generator=gen, dtype=torch.float32) * (hi - lo) + lo
+    return v.to(td)

@@ -172,6 +172,20 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
                        int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                        gemm_epilogue_t epi, int stages, void* stream);
 
+/* As gemm_run, with a per-column bias:
+ *   C[i,j] = epi(sum_k A[i,k] B[j,k] + bias[j]).
+ * bias: device pointer to N values of `dtype` (2-byte aligned, not
+ * overlapping C), or NULL for none (then the same as gemm_run).  The bias is
+ * added to the fp32 accumulator, after any stream-K partial and before the
+ * epilogue function.  With K == 0, C = epi(bias) in every row.
+ *
+ * The pages define no bias term.  This is the reading of a Linear layer's
+ * bias (the GELU workload, Y = gelu(X . W^T), is such a layer): one value per
+ * output feature, i.e. per column of C. */
+gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, const void* bias,
+                            void* C, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                            gemm_epilogue_t epi, int stages, void* stream);
+
 /* End-to-end call with HOST buffers: copies hA (M*K) and hB (N*K) to
  * plan-owned device buffers, runs the GEMM on `stream`, copies C back to hC
  * (M*N) and synchronises `stream` before returning.  Pinned host memory gives

@@ -27,7 +27,8 @@ from typing import Optional
 
 __all__ = [
     "GemmError", "Plan", "matmul_nt", "matmul_nn", "load_library", "library_path",
-    "gemm_plan_create", "gemm_plan_create_ex", "gemm_run", "gemm_run_host", "gemm_plan_check",
+    "gemm_plan_create", "gemm_plan_create_ex", "gemm_run", "gemm_run_bias", "gemm_run_host",
+    "gemm_plan_check",
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
@@ -117,6 +118,8 @@ def load_library(path: Optional[str] = None):
         lib.gemm_plan_create_ex.restype = ci
         lib.gemm_run.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
         lib.gemm_run.restype = ci
+        lib.gemm_run_bias.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
+        lib.gemm_run_bias.restype = ci
         lib.gemm_run_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
         lib.gemm_run_host.restype = ci
         lib.gemm_plan_check.argtypes = [vp, ctypes.POINTER(ctypes.c_int32),
@@ -189,6 +192,11 @@ def gemm_plan_create_ex(M, N, K, dtype, epi, stages, variant, device, tuning=Non
 def gemm_run(plan, A, B, C, M, N, K, dtype, epi, stages, stream):
     """A, B, C, stream: integer addresses / handles.  Returns the status."""
     return load_library().gemm_run(plan, A, B, C, M, N, K, dtype, epi, stages, stream)
+
+
+def gemm_run_bias(plan, A, B, bias, C, M, N, K, dtype, epi, stages, stream):
+    """As gemm_run, plus a device pointer to N bias values (or None)."""
+    return load_library().gemm_run_bias(plan, A, B, bias, C, M, N, K, dtype, epi, stages, stream)
 
 
 def gemm_run_host(plan, hA, hB, hC, M, N, K, dtype, epi, stages, stream):
@@ -264,15 +272,23 @@ class Plan:
         _check(st, "gemm_plan_get_info")
         return info.as_dict()
 
-    def run_ptr(self, A: int, B: int, C: int, stream: int = 0):
-        _check(gemm_run(self._h, A, B, C, self.M, self.N, self.K, self.dtype, self.epi,
-                        self.stages, stream), "gemm_run")
+    def run_ptr(self, A: int, B: int, C: int, stream: int = 0, bias: int = 0):
+        """Device addresses; bias: address of N bias values, or 0 for none."""
+        if bias:
+            _check(gemm_run_bias(self._h, A, B, bias, C, self.M, self.N, self.K, self.dtype,
+                                 self.epi, self.stages, stream), "gemm_run_bias")
+        else:
+            _check(gemm_run(self._h, A, B, C, self.M, self.N, self.K, self.dtype, self.epi,
+                            self.stages, stream), "gemm_run")
 
-    def run(self, A, B, C, stream=None):
-        """A, B, C: torch CUDA tensors (contiguous, shapes (M,K), (N,K), (M,N))."""
+    def run(self, A, B, C, stream=None, bias=None):
+        """A, B, C: torch CUDA tensors (contiguous, shapes (M,K), (N,K) -- or
+        (K,N) with b_kn -- and (M,N)); bias: None or a contiguous (N,) tensor
+        of A's dtype on the same device."""
         import torch
         s = stream if stream is not None else torch.cuda.current_stream(A.device)
-        self.run_ptr(A.data_ptr(), B.data_ptr(), C.data_ptr(), s.cuda_stream)
+        self.run_ptr(A.data_ptr(), B.data_ptr(), C.data_ptr(), s.cuda_stream,
+                     bias.data_ptr() if bias is not None else 0)
 
     def run_host(self, hA: int, hB: int, hC: int, stream: int = 0):
         _check(gemm_run_host(self._h, hA, hB, hC, self.M, self.N, self.K, self.dtype, self.epi,
@@ -300,15 +316,16 @@ _plans = {}
 _plans_lock = threading.Lock()
 
 
-def matmul_nn(A, B, epilogue=None, stages: int = 6, out=None, out_dtype=None, **tuning):
-    """C = epi(A @ B) on the current CUDA stream, B stored (K, N) row-major.
+def matmul_nn(A, B, epilogue=None, stages: int = 6, out=None, out_dtype=None, bias=None,
+              **tuning):
+    """C = epi(A @ B + bias) on the current CUDA stream, B stored (K, N) row-major.
 
     The [M, K] @ [K, N] form of the Mosaic GPU pipelining guide's example;
     same arguments and checks as :func:`matmul_nt` otherwise."""
     if B.dim() != 2 or A.dim() != 2 or A.shape[1] != B.shape[0]:
         raise ValueError("A must be (M, K) and B (K, N) with the same K")
     return matmul_nt(A, B, epilogue=epilogue, stages=stages, out=out, out_dtype=out_dtype,
-                     _b_kn=True, **tuning)
+                     bias=bias, _b_kn=True, **tuning)
 
 
 def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
@@ -323,11 +340,12 @@ def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", devic
 
 
 def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", out=None,
-              out_dtype=None, **tuning):
-    """C = epi(A @ B.T) on the current CUDA stream.
+              out_dtype=None, bias=None, **tuning):
+    """C = epi(A @ B.T + bias) on the current CUDA stream.
 
     A: (M, K) and B: (N, K) CUDA tensors of the same dtype (float16 or
-    bfloat16), contiguous.  epilogue: None, "gelu" or "relu".  Returns C
+    bfloat16), contiguous.  epilogue: None, "gelu" or "relu".  bias: None or
+    an (N,) tensor of that dtype, added before the epilogue.  Returns C
     (M, N) of that dtype, or of float32 when out_dtype is torch.float32
     (``out`` if given).  ``tuning`` keywords go to :class:`Plan` (tile_n,
     cta_group, raster_group, max_ctas, tail_split, timeout_ns); plans are
@@ -360,6 +378,10 @@ def matmul_nt(A, B, epilogue=None, stages: int = 6, variant: str = "pipelined", 
     dtype = "bf16" if dt == GEMM_BF16 else "f16"
     if c_dtype == torch.float32:
         tuning["out_f32"] = 1
+    if bias is not None and (not bias.is_cuda or bias.dtype != A.dtype or bias.dim() != 1
+                             or bias.shape[0] != N or not bias.is_contiguous()
+                             or bias.device != A.device):
+        raise ValueError("bias must be a contiguous (N,) CUDA tensor of A's dtype and device")
     plan = get_plan(M, N, K, dtype, epilogue, stages, variant, A.device.index or 0, **tuning)
-    plan.run(A, B, out)
+    plan.run(A, B, out, bias=bias)
     return out

@@ -24,7 +24,7 @@ LIB = os.path.join(LIBDIR, "libspgemm.so")
 STAMP = os.path.join(LIBDIR, "libspgemm.stamp")
 
 SOURCES = ["gemm_api.cu", "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu", "gemm_pair128.cu",
-           "gemm_pair256.cu", "pad.cu", "noalloc.cu"]
+           "gemm_pair256.cu", "pad.cu", "fill.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]
@@ -50,7 +50,8 @@ def _digest() -> str:
     return h.hexdigest()
 
 
-KERNEL_FILES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "gemm_instance.cuh",
+KERNEL_FILES = ["gemm_kernel.cuh", "epilogue_math.cuh", "ptx.cuh", "kernel_params.h",
+                "gemm_instance.cuh",
                 "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu", "gemm_pair128.cu",
                 "gemm_pair256.cu"]
 

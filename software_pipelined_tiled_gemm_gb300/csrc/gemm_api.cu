@@ -588,6 +588,12 @@ gemm_status_t gemm_plan_create(gemm_plan_t** out, int64_t M, int64_t N, int64_t 
 gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C, int64_t M,
                        int64_t N, int64_t K, gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
                        void* stream_handle) {
+  return gemm_run_bias(plan, A, B, nullptr, C, M, N, K, dtype, epi, stages, stream_handle);
+}
+
+gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, const void* bias,
+                            void* C, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                            gemm_epilogue_t epi, int stages, void* stream_handle) {
   g_last_error.clear();
   if (!plan) return fail(GEMM_ERR_INVALID_ARG, "plan is NULL");
   gemm_status_t st = check_common(M, N, K, dtype, epi, stages);
@@ -611,9 +617,13 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   const size_t bytesC = static_cast<size_t>(M) * N * esC;
   if (ranges_overlap(C, bytesC, A, bytesA) || ranges_overlap(C, bytesC, B, bytesB))
     return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
-  if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u) ||
+  if (bias && ranges_overlap(C, bytesC, bias, static_cast<size_t>(N) * 2))
+    return fail(GEMM_ERR_INVALID_ARG, "C overlaps the bias");
+  if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+        reinterpret_cast<uintptr_t>(bias)) & 1u) ||
       (reinterpret_cast<uintptr_t>(C) & (esC - 1)) != 0)
-    return fail(GEMM_ERR_INVALID_ARG, "A and B must be 2-byte and C %zu-byte aligned", esC);
+    return fail(GEMM_ERR_INVALID_ARG, "A, B and the bias must be 2-byte and C %zu-byte aligned",
+                esC);
 
   DeviceGuard guard(plan->device);
   if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
@@ -624,7 +634,15 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
     ~NvtxRange() { nvtxRangePop(); }
   } nvtx_range;
 
-  if (K == 0) {  // empty reduction: C = 0, and GELU(0) = 0
+  if (K == 0) {  // empty reduction: C = epi(bias), or 0 (GELU(0) = ReLU(0) = 0)
+    if (bias) {
+      cudaError_t e = launch_bias_fill(C, M, N, bias, plan->dtype == GEMM_BF16,
+                                       static_cast<int>(plan->epi), plan->out_f32 != 0,
+                                       plan->sm_count, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "bias fill launch");
+      plan->last_kernels = 1;
+      return GEMM_OK;
+    }
     cudaError_t e = cudaMemsetAsync(C, 0, bytesC, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     plan->last_kernels = 0;
@@ -793,6 +811,7 @@ gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
   prm.sk_tiles = static_cast<int>(plan->sk_tiles);
   prm.sk_ws = plan->sk_ws;
   prm.sk_flags = plan->sk_flags;
+  prm.bias = bias;
 
   cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC,
                          plan->tmBp, prm, plan->grid, plan->smem, stream);

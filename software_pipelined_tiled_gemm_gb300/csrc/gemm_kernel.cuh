@@ -23,10 +23,11 @@
 //                       unit's last slot: commit -> tmem_full[acc].
 //   warps 2-5           epilogue: wait tmem_full[acc]; for stream-K owners,
 //                       add the other walker's fp32 partial; then tcgen05.ld
-//                       32 rows x 64 columns per step, apply the epilogue
-//                       function, round, write a swizzled staging tile and
-//                       send it out with a TMA store (or row-wise stores when
-//                       C's pitch is not 16-byte aligned); then arrive on
+//                       32 rows x 64 columns per step, add the bias (if
+//                       any), apply the epilogue function, round, write a
+//                       swizzled staging tile and send it out with a TMA
+//                       store (or row-wise stores when C's pitch is not
+//                       16-byte aligned); then arrive on
 //                       tmem_empty[acc].
 //
 // With two TMEM accumulators the epilogue of one unit overlaps the main loop
@@ -49,6 +50,7 @@
 
 #include <cstdint>
 
+#include "epilogue_math.cuh"
 #include "kernel_params.h"
 #include "ptx.cuh"
 
@@ -58,12 +60,19 @@ static __device__ __noinline__ void record_error(int* status, int code, int deta
   if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
 }
 
+// Suspend-time hint of the long waits (an epilogue warp waits for most of a
+// tile's main loop): wake on the phase, not on a short default limit.
+constexpr uint32_t kLongWaitHintNs = 1000000u;
+
 // Wait for the phase of parity `parity` of barrier `bar`; false on timeout.
+// kLong: the wait is expected to be long (suspend-time hint).
+template <bool kLong = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p,
                                              int detail) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!(kLong ? ptx::mbar_try_wait_sleep(bar, parity, kLongWaitHintNs)
+                 : ptx::mbar_try_wait(bar, parity))) {
     if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       record_error(p.status, kStatusTimeout, detail);
       return false;
@@ -190,16 +199,6 @@ __device__ __forceinline__ int k_start(const Unit& x, int walker, int walkers, c
   return static_cast<int>((static_cast<int64_t>(idx) * p.k_blocks) / n);
 }
 
-__device__ __forceinline__ float gelu_tanh(float x) {
-  // 0.5 x (1 + tanh(u)) == x / (1 + exp(-2u)), u = 0.7978845608 (x + 0.044715 x^3);
-  // this form cannot produce inf/inf for large |u| (x -> x for u -> +inf,
-  // x -> -0 for u -> -inf).  CUDA's fast exponential and division keep the
-  // epilogue cheap; their few-ulp fp32 error is far below the 8/11-bit
-  // precision of the rounded output, and __fdividef(x, inf) gives -0/+0.
-  const float inner = x * fmaf(0.044715f, x * x, 1.0f);
-  return __fdividef(x, 1.0f + __expf(-1.5957691216f * inner));
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -207,6 +206,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Bias of one column (0 at or beyond N), as fp32.  Lane l fetches the
+// columns col0 + l and col0 + 32 + l of a 64-column chunk: two coalesced
+// 64-byte loads per warp, issued one chunk ahead of their use.
+__device__ __forceinline__ float load_bias(const Params& p, int col, bool bf16) {
+  if (col >= p.N) return 0.0f;
+  const unsigned short bits = __ldg(static_cast<const unsigned short*>(p.bias) + col);
+  return bf16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+}
+
+// r[j] += the bias of column j of the 32 (lane j holds it in `b`): every row
+// (lane) adds the same 32 values, handed round by warp shuffles.
+__device__ __forceinline__ void add_bias32(uint32_t (&r)[32], float b) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    r[j] = __float_as_uint(__uint_as_float(r[j]) + __shfl_sync(0xffffffffu, b, j));
 }
 
 // Epilogue function EPI on 32 fp32 accumulator values held as raw words:
@@ -219,7 +235,7 @@ __device__ __forceinline__ void apply_epilogue32(uint32_t (&r)[32]) {
   for (int j = 0; j < 32; ++j) {
     float x = __uint_as_float(r[j]);
     if constexpr (EPI == 1) x = gelu_tanh(x);
-    if constexpr (EPI == 2) x = x > 0.0f ? x : 0.0f;
+    if constexpr (EPI == 2) x = relu(x);
     r[j] = __float_as_uint(x);
   }
 }
@@ -567,8 +583,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_width = narrow ? BN / p.tail_splits : BN;
       const int n0 = nb * BN + (narrow ? x.sub * n_width : 0);
       const uint32_t chunks = static_cast<uint32_t>(n_width) / kStoreCols;
+      // Bias of the first 64-column chunk, fetched before the accumulator
+      // wait so its latency hides there (later chunks: one chunk ahead).
+      float nb0 = 0.0f, nb1 = 0.0f;
+      if (p.bias != nullptr && x.role != kContrib) {
+        nb0 = load_bias(p, n0 + lane, bf16);
+        nb1 = load_bias(p, n0 + 32 + lane, bf16);
+      }
       int ready = 1;
-      if (lane == 0) ready = wait_bounded(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
+      if (lane == 0) ready = wait_bounded<true>(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
       ready = __shfl_sync(0xffffffffu, ready, 0);
       if (!ready) break;
       ptx::tc_fence_after_sync();
@@ -622,6 +645,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t c = 0; c < chunks; ++c) {
           const int col0 = n0 + static_cast<int>(c) * kStoreCols;
           if (col0 >= p.N) break;
+          const float b0 = nb0, b1 = nb1;
+          if (p.bias != nullptr && c + 1 < chunks) {
+            nb0 = load_bias(p, col0 + kStoreCols + lane, bf16);
+            nb1 = load_bias(p, col0 + kStoreCols + 32 + lane, bf16);
+          }
           uint32_t r0[32], r1[32];
           ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols, r0);
           ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols + 32, r1);
@@ -634,6 +662,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               r0[j] = __float_as_uint(__uint_as_float(r0[j]) + fix[(cb + j) * 32 + lane]);
               r1[j] = __float_as_uint(__uint_as_float(r1[j]) + fix[(cb + 32 + j) * 32 + lane]);
             }
+          }
+          if (p.bias != nullptr) {  // after the partial: a fixed order on every run
+            add_bias32(r0, b0);
+            add_bias32(r1, b1);
           }
           // Epilogue function on the fp32 accumulator values.
           if (p.epilogue == 1) {

@@ -95,6 +95,9 @@ struct Params {
   int b_kn;
   // 64-wide K slices per ring slot (1 or 2); stages and k_blocks count slots.
   int k_sub;
+  // Per-column bias (N values of the input type), added to the fp32
+  // accumulator before the epilogue function; nullptr for none.
+  const void* bias;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
   // copies of its first K slice (see gemm_tuning_t::debug_fault).
   int inject_fault;

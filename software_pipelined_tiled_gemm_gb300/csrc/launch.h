@@ -40,4 +40,9 @@ cudaError_t launch_pad_operands(const uint16_t* A, int64_t M, uint16_t* Ap, cons
                                 int64_t N, uint16_t* Bp, int64_t K, int64_t Kp, int sm_count,
                                 cudaStream_t stream);
 
+// K = 0 with a bias: C[i, j] = epi(bias[j]) for an M x N C with pitch N
+// (fp32, or the input type); bias holds N fp16/bf16 values.
+cudaError_t launch_bias_fill(void* C, int64_t M, int64_t N, const void* bias, bool bf16,
+                             int epilogue, bool out_f32, int sm_count, cudaStream_t stream);
+
 }  // namespace spgemm

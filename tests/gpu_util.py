@@ -17,7 +17,8 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 
 def run_device(A: torch.Tensor, B: torch.Tensor, dtype: str, epilogue=None, stages=4,
-               variant="pipelined", c_offset=0, a_offset=0, b_offset=0, fill=0xFFFF, **tuning):
+               variant="pipelined", c_offset=0, a_offset=0, b_offset=0, fill=0xFFFF, bias=None,
+               **tuning):
     """Run C = epi(A.B^T) on cuda:0 through gemm_run (C = epi(A.B) with B of
     shape (K, N) when tuning has b_kn=1).
 
@@ -38,13 +39,17 @@ def run_device(A: torch.Tensor, B: torch.Tensor, dtype: str, epilogue=None, stag
 
     _, a = place(A, a_offset)
     _, b = place(B, b_offset)
+    bias_ptr = 0
+    if bias is not None:
+        _, bd = place(bias, 0)
+        bias_ptr = bd.data_ptr()
     cbuf = torch.empty(M * N + c_offset + 64, dtype=_TD[dtype], device=dev)
     cbuf.view(torch.int16).fill_(np.int16(np.uint16(fill).view(np.int16)).item())
     c = cbuf[c_offset:c_offset + M * N]
     plan = sg.Plan(M, N, K, dtype, epilogue, stages, variant, 0, **tuning)
     try:
         stream = torch.cuda.current_stream(dev)
-        plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), stream.cuda_stream)
+        plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), stream.cuda_stream, bias_ptr)
         torch.cuda.synchronize(dev)
         ds, detail = plan.check()
         assert ds == 0, "device status %d detail %#x" % (ds, detail)
@@ -57,14 +62,14 @@ def run_device(A: torch.Tensor, B: torch.Tensor, dtype: str, epilogue=None, stag
     return out, info, canary_ok
 
 
-def check_full(A, B, dtype, C, epilogue=None):
-    ref = oracle.gemm_nt(A, B, dtype, epilogue=epilogue)
+def check_full(A, B, dtype, C, epilogue=None, bias=None):
+    ref = oracle.gemm_nt(A, B, dtype, epilogue=epilogue, bias=bias)
     got = oracle.decode(bits(C), dtype)
     return tolerance.compare(got, ref, dtype), ref, got
 
 
-def check_sampled(A, B, dtype, C, rows, cols, epilogue=None):
-    ref = oracle.gemm_nt_entries(A, B, dtype, rows, cols, epilogue=epilogue)
+def check_sampled(A, B, dtype, C, rows, cols, epilogue=None, bias=None):
+    ref = oracle.gemm_nt_entries(A, B, dtype, rows, cols, epilogue=epilogue, bias=bias)
     got = oracle.decode(bits(C)[rows, cols], dtype)
     return tolerance.compare(got, ref, dtype)
 

@@ -91,6 +91,7 @@ def test_null_out_pointer_rejected():
 def test_null_plan_rejected_everywhere():
     assert sg.gemm_run(None, 1, 2, 3, 8, 8, 8, 0, 0, 4, None) == sg.GEMM_ERR_INVALID_ARG
     assert sg.gemm_run_host(None, 1, 2, 3, 8, 8, 8, 0, 0, 4, None) == sg.GEMM_ERR_INVALID_ARG
+    assert sg.gemm_run_bias(None, 1, 2, 4, 3, 8, 8, 8, 0, 0, 4, None) == sg.GEMM_ERR_INVALID_ARG
     st, _, _ = sg.gemm_plan_check(None)
     assert st == sg.GEMM_ERR_INVALID_ARG
     st, _ = sg.gemm_plan_get_info(None)
