@@ -2,7 +2,8 @@
 
 Each case draws M, N, K (1 .. ~700), the dtype, the epilogue, the B layout,
 the CTA group, the ring depth, the last-wave scheme, fp32 output and
-unaligned operand bases, runs the CUDA path through the C ABI and compares
+unaligned operand bases (every third case also adds a per-column bias),
+runs the CUDA path through the C ABI and compares
 every element with the fp64 oracle (2 ulp + 1e-3 per element, relative
 Frobenius 1e-3).  Option combinations the planner rejects by design (for
 example narrow tail tiles with a K x N B, or a ring that does not fit shared
@@ -55,7 +56,7 @@ def _draw(rng):
     }
 
 
-def _run_case(cfg):
+def _run_case(cfg, with_bias=False):
     import software_pipelined_tiled_gemm_gb300 as sg
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     dtype, epi = cfg["dtype"], cfg["epilogue"]
@@ -77,6 +78,8 @@ def _run_case(cfg):
         view.copy_(x.reshape(-1).to(dev))
         return buf, view
 
+    bias = gemm_inputs.bias(N, dtype, seed=M + N + K) if with_bias else None
+    bias_d = bias.to(dev) if with_bias else None
     Bd = B.t().contiguous() if cfg["b_kn"] else B
     _, a = place(A, a_off, td)
     _, b = place(Bd, b_off, td)
@@ -86,14 +89,15 @@ def _run_case(cfg):
                    "single_buffer" if cfg["stages"] == 1 else "pipelined", 0, **tuning)
     try:
         plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(),
-                     torch.cuda.current_stream(dev).cuda_stream)
+                     torch.cuda.current_stream(dev).cuda_stream,
+                     bias_d.data_ptr() if with_bias else 0)
         torch.cuda.synchronize(dev)
         ds, detail = plan.check()
         assert ds == 0, "device status %d detail %#x" % (ds, detail)
         info = plan.info()
     finally:
         plan.close()
-    ref = oracle.gemm_nt(A, B, dtype, epilogue=epi)
+    ref = oracle.gemm_nt(A, B, dtype, epilogue=epi, bias=bias)
     if cfg["out_f32"]:
         got = c.view(M, N).cpu().double().numpy()
         st = tolerance.compare(got, ref, "f32")
@@ -114,7 +118,7 @@ def test_random_configurations_match_the_oracle(seed):
     for i in range(N_CASES):
         cfg = _draw(rng)
         try:
-            st, info = _run_case(cfg)
+            st, info = _run_case(cfg, with_bias=i % 3 == 0)
         except sg.GemmError as e:
             if e.status in (sg.GEMM_ERR_INVALID_ARG, sg.GEMM_ERR_SMEM_BUDGET):
                 skipped += 1
