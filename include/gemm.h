@@ -118,6 +118,12 @@ typedef struct {
                           never receives its first K slice, so the pipeline's waits run
                           out their time limit and gemm_plan_check reports
                           GEMM_ERR_TIMEOUT (every other tile still completes) */
+  int k_serpentine;    /* K order of successive waves of tiles: 0 = auto (alternate when
+                          the A and B rows one wave of tiles reads exceed half of L2),
+                          1 = alternate (a CTA's odd-numbered tiles walk K downwards, so
+                          the next wave starts on the slices the last one read most
+                          recently), -1 = always upwards.  Ignored for a single row of
+                          tiles, whose K loops are staggered instead */
 } gemm_tuning_t;
 
 /* Read-only description of what a plan will launch (for tests and benchmarks). */
@@ -144,6 +150,7 @@ typedef struct {
                                   slots of k_sub slices each (same shared memory) */
   int host_panels;             /* row panels gemm_run_host pipelines its copies in
                                   (0 before the first pipelined call) */
+  int k_serpentine;            /* 1: successive waves alternate their K direction */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

@@ -427,7 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             CG * kSub;
         const int nk = x.k1 - x.k0;
         const int kr = k_start(x, walker, walkers, p);
-        for (int i = 0, kb = x.k0 + kr; i < nk; ++i, kb = (kb + 1 == x.k1) ? x.k0 : kb + 1) {
+        const bool down = p.k_serpentine && (x.seq & 1) && x.role == kWhole;
+        for (int i = 0, kf = x.k0 + kr; i < nk; ++i, kf = (kf + 1 == x.k1) ? x.k0 : kf + 1) {
+          const int kb = down ? x.k1 - 1 - i : kf;  // K slot this iteration copies
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
             ok = false;
             break;

@@ -77,6 +77,11 @@ struct Params {
   // so CTAs that share the same A rows do not all read the same A slice at
   // the same time (used when a single row of tiles spans the whole grid).
   int k_rotate;
+  // 1: a walker's odd-numbered units (x.seq odd) load their K slices in
+  // descending order, so each wave of tiles begins on the slices the previous
+  // wave read last, which are the ones most likely still in L2.  Only the
+  // copy order changes: the MMA loop counts iterations, not slice indexes.
+  int k_serpentine;
   // > 0: the producer also prefetches B into L2, prefetch_kb slices ahead,
   // through a tensor map whose box spans 4 K slices (512 contiguous bytes of
   // each row): memory-bound shapes then read B in longer runs.
