@@ -151,6 +151,9 @@ typedef struct {
   int host_panels;             /* row panels gemm_run_host pipelines its copies in
                                   (0 before the first pipelined call) */
   int k_serpentine;            /* 1: successive waves alternate their K direction */
+  int l2_prefetch_first;       /* 1: operands exceed 3/4 of L2, so each CTA prefetches its first
+                                  ring's slices into L2 before waiting on the previous
+                                  kernel in the stream */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

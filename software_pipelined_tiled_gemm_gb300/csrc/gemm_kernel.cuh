@@ -384,6 +384,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tmB);
     if (kSplit) ptx::tma_prefetch_desc(&tmBt);
     if (p.tma_store) ptx::tma_prefetch_desc(&tmC);
+    // Warm L2 with the slices the ring will hold first (operands that do not
+    // stay in L2, see Params::l2_prefetch_first).  This runs before
+    // the wait on the previous kernel and only moves lines into L2, the
+    // device's point of coherence: a line the previous kernel still writes
+    // is updated there, and the ring's own copies are issued after the wait.
+    UnitIter it0(walker, walkers, p);
+    Unit x0;
+    if (p.l2_prefetch_first && it0.next(p, x0)) {
+      int mb, nb;
+      tile_coords(x0.tile, p, mb, nb);
+      const bool narrow = kSplit && x0.sub >= 0;
+      const int n_width = narrow ? BN / p.tail_splits : BN;
+      const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
+      const int b_row = nb * BN + (narrow ? x0.sub * n_width : 0) + static_cast<int>(rank) * (n_width / CG);
+      const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
+      const int nk = x0.k1 - x0.k0;
+      const int kr = k_start(x0, walker, walkers, p);
+      for (int i = 0; i < S && i < nk; ++i) {
+        const int kb = x0.k0 + (kr + i) % nk;
+#pragma unroll
+        for (int sub = 0; sub < kSub; ++sub) {
+          const int kx = (kb * kSub + sub) * kBK;
+          ptx::tma_prefetch_l2_2d(&tmA, kx, a_row);
+          if constexpr (!kKN)
+            ptx::tma_prefetch_l2_2d(tmb, kx, b_row);
+          else
+            ptx::tma_prefetch_l2_4d(tmb, 0, 0, b_row / 64, kx / 8);
+        }
+      }
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), tmem_cols);

@@ -82,6 +82,11 @@ struct Params {
   // wave read last, which are the ones most likely still in L2.  Only the
   // copy order changes: the MMA loop counts iterations, not slice indexes.
   int k_serpentine;
+  // 1: before waiting on the previous kernel, the producer prefetches into L2
+  // the slices its ring will hold first (operands above 3/4 of L2, whose
+  // first slices come from DRAM; for L2-resident operands the prefetches
+  // only delay the ring's own copies).
+  int l2_prefetch_first;
   // > 0: the producer also prefetches B into L2, prefetch_kb slices ahead,
   // through a tensor map whose box spans 4 K slices (512 contiguous bytes of
   // each row): memory-bound shapes then read B in longer runs.

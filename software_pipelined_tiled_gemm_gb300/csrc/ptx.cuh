@@ -131,6 +131,14 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap,
 }
 
 // Prefetch the 2-D box at (x, y) into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const void* tmap, int32_t x, int32_t y,
+                                                   int32_t z, int32_t w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),

@@ -97,6 +97,24 @@ def test_serpentine_planner_choice():
         serp(512, 512, 512, k_serpentine=2)
 
 
+def test_l2_prefetch_planner_choice():
+    # the first ring's slices are prefetched into L2 only for operands that do
+    # not stay in L2 (above 3/4 of it: GB300 reports 135.5 MB)
+    import software_pipelined_tiled_gemm_gb300 as sg
+
+    def pf(M, N, K):
+        p = sg.Plan(M, N, K, "f16", None, 6, "pipelined", 0)
+        try:
+            return p.info()["l2_prefetch_first"]
+        finally:
+            p.close()
+
+    assert pf(64, 8192, 8192) == 1        # 135 MB of operands
+    assert pf(8192, 8192, 8192) == 1
+    assert pf(4096, 4096, 4096) == 0      # 64 MB: L2-resident
+    assert pf(16896, 512, 640) == 0
+
+
 def test_serpentine_order_is_deterministic():
     # same plan, same inputs: identical bits on every run
     import software_pipelined_tiled_gemm_gb300 as sg
