@@ -154,6 +154,9 @@ typedef struct {
   int l2_prefetch_first;       /* 1: operands exceed 3/4 of L2, so each CTA prefetches its first
                                   ring's slices into L2 before waiting on the previous
                                   kernel in the stream */
+  int sk_cluster;              /* 1: every tile is split into two K halves on the two CTAs
+                                  of a cluster, whose partial sum moves through
+                                  distributed shared memory */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

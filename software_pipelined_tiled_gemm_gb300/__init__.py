@@ -76,7 +76,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("tail_splits", ctypes.c_int), ("work_units", ctypes.c_int64),
                 ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int), ("b_kn", ctypes.c_int),
                 ("k_sub", ctypes.c_int), ("host_panels", ctypes.c_int),
-                ("k_serpentine", ctypes.c_int), ("l2_prefetch_first", ctypes.c_int)]
+                ("k_serpentine", ctypes.c_int), ("l2_prefetch_first", ctypes.c_int),
+                ("sk_cluster", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -122,6 +122,7 @@ struct gemm_plan {
   int k_sub = 1;                 // 64-wide K slices per ring slot
   int k_serpentine = 0;          // odd waves walk K downwards
   int l2_prefetch_first = 0;     // prefetch the first ring's slices before the PDL wait
+  int sk_cluster = 0;            // K halves exchanged within 2-CTA clusters
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -495,6 +496,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     p->dp_tiles = 0;
     p->sk_tiles = p->num_tiles;
     walkers = static_cast<int>(2 * p->num_tiles);
+    // Walkers 2t (first half, owner) and 2t + 1 (second half) are adjacent
+    // CTAs: launched as 2-CTA clusters, the partial goes through distributed
+    // shared memory instead of a workspace round trip through L2.
+    p->sk_cluster = 1;
   } else if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
     const int64_t rem = p->num_tiles % walkers;
     const int64_t ring = static_cast<int64_t>(stages) *
@@ -837,6 +842,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.k_rotate = (plan->tiles_m == 1 && plan->num_tiles > 1) ? 1 : 0;
   prm.k_serpentine = plan->k_serpentine;
   prm.l2_prefetch_first = plan->l2_prefetch_first;
+  prm.sk_cluster = plan->sk_cluster;
   prm.inject_fault = plan->debug_fault;
   prm.prefetch_kb = plan->prefetch_kb;
   prm.a_box_rows = static_cast<int>(a_box_rows);
@@ -1057,6 +1063,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->sm_count = plan->sm_count;
   info->k_serpentine = plan->k_serpentine;
   info->l2_prefetch_first = plan->l2_prefetch_first;
+  info->sk_cluster = plan->sk_cluster;
   info->cta_group = plan->cg;
   info->tail_tiles = plan->num_tiles - plan->dp_tiles;
   info->tail_splits = plan->tail_splits;

@@ -76,8 +76,10 @@ cudaError_t launch_instance(const cudaLaunchConfig_t& cfg, const CUtensorMap& a,
 }
 
 // Launch configuration: `grid` CTAs of kThreads threads, programmatic
-// dependent launch allowed, and clusters of 2 CTAs for pairs.
-inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int cg, int grid,
+// dependent launch allowed, and clusters of `cluster` (1 or 2) CTAs: 2 for
+// pairs and for single CTAs whose tiles are split in two K halves within a
+// cluster (Params::sk_cluster).
+inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int cluster, int grid,
                         size_t smem, cudaStream_t stream) {
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -85,7 +87,7 @@ inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int 
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int n = 0;
-  if (cg == 2) {
+  if (cluster == 2) {
     attr[n].id = cudaLaunchAttributeClusterDimension;
     attr[n].val.clusterDim.x = 2;
     attr[n].val.clusterDim.y = 1;
@@ -110,7 +112,7 @@ inline void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int 
                                  cudaStream_t stream) {                                        \
     cudaLaunchConfig_t cfg;                                                                    \
     cudaLaunchAttribute attr[2];                                                               \
-    make_config(cfg, attr, 1, grid, smem, stream);                                             \
+    make_config(cfg, attr, p.sk_cluster ? 2 : 1, grid, smem, stream);                          \
     return launch_instance<BN, 1>(cfg, a, b, bt, c, bp, p);                                    \
   }                                                                                            \
   }

@@ -353,8 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + 2 + a); };
   const uint32_t done_bar = bar_base + 8u * (2 * kMaxStages + 4);
   auto fix_bar = [&](int q) { return bar_base + 8u * (2 * kMaxStages + 5 + q); };
+  // Cluster split: the owner tells the contributor its ring is free.
+  auto free_bar = [&](int q) { return bar_base + 8u * (2 * kMaxStages + 9 + q); };
   uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 9));
+      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 13));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -376,7 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty_bar(a), kEpiWarps * CG);
     }
     ptx::mbar_init(done_bar, 1);
-    for (int q = 0; q < kEpiWarps; ++q) ptx::mbar_init(fix_bar(q), 1);
+    for (int q = 0; q < kEpiWarps; ++q) {
+      ptx::mbar_init(fix_bar(q), 1);
+      ptx::mbar_init(free_bar(q), 1);
+    }
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -420,8 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_relinquish<CG>();
   }
   ptx::tc_fence_before_sync();
-  if constexpr (CG == 2)
-    ptx::cluster_sync();  // peer barriers initialised before any remote arrive / TMA
+  // Peer barriers must be initialised before any remote arrive / TMA.
+  if (CG == 2 || (kSplit && p.sk_cluster))
+    ptx::cluster_sync();
   else
     __syncthreads();
   ptx::tc_fence_after_sync();
@@ -639,7 +645,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                            ? p.sk_ws + static_cast<size_t>(flag_idx) * (kWarpPartial / 4u)
                            : nullptr;
       bool have_partial = false;
-      if (kSplit && x.role == kContrib) {
+      if (kSplit && x.role == kContrib && p.sk_cluster) {
+        // Cluster split: stage this warp's partial in this CTA's own idle
+        // ring ([column][lane], the layout the owner reads), then, once the
+        // owner's ring is free, bulk-copy it there; the bytes complete the
+        // owner's fix-up barrier.  Rows >= M are never stored, so their warps
+        // exchange nothing.  The final cluster barrier keeps this CTA (the
+        // copy's source) alive until the owner has received the bytes.
+        if (row0 < p.M) {
+          float* stage_out = reinterpret_cast<float*>(smem + q * kWarpPartial);
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c, v);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stage_out[(c + j) * 32 + lane] = __uint_as_float(v[j]);
+          }
+          ptx::fence_proxy_async_smem();  // generic writes -> the copy engine
+          __syncwarp();
+          int ok = 1;
+          if (lane == 0) {
+            // A walker holds one unit in this mode, so the barrier's first phase.
+            ok = wait_bounded_cluster<2>(free_bar(q), 0, p, kDetailSkFree) ? 1 : 0;
+            if (ok)
+              ptx::bulk_copy_to_peer(ptx::map_shared_rank(sbase + q * kWarpPartial, 0),
+                                     sbase + q * kWarpPartial, kWarpPartial,
+                                     ptx::map_shared_rank(fix_bar(q), 0));
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+        }
+      } else if (kSplit && x.role == kContrib) {
         // Publish the partial sum of K slices [k0, k1) and raise the flag.
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -652,6 +689,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) atomicAdd(p.sk_flags + flag_idx, 1);
+      } else if (kSplit && x.role == kOwner && p.sk_cluster) {
+        // Cluster split: this walker's MMAs are done (accumulator full), so
+        // its ring is idle; let the contributor copy its partial there.
+        if (row0 < p.M) {
+          int ok = 1;
+          if (lane == 0) {
+            // Arm the fix-up barrier for the partial's bytes before telling
+            // the contributor that the ring may be written.
+            ptx::mbar_arrive_expect_tx(fix_bar(q), kWarpPartial);
+            ptx::mbar_arrive_cluster(ptx::map_shared_rank(free_bar(q), 1));
+            ok = wait_bounded_cluster<2>(fix_bar(q), fix_phase, p, kDetailSkCopy) ? 1 : 0;
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          // Every lane acquires the contributor's writes (the phase is complete).
+          (void)ptx::mbar_try_wait_cluster(fix_bar(q), fix_phase);
+          fix_phase ^= 1u;
+          have_partial = true;
+        }
       } else if (kSplit && x.role == kOwner) {
         // The other walker's partial (K slices [k1, k_blocks)) was written at
         // the start of its range.  This is the last unit of this walker, so
@@ -744,8 +800,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before_sync();
-  if constexpr (CG == 2)
-    ptx::cluster_sync();  // neither CTA leaves while its peer may still touch its memory
+  // Neither CTA of a cluster leaves while its peer may still touch its memory.
+  if (CG == 2 || (kSplit && p.sk_cluster))
+    ptx::cluster_sync();
   else
     __syncthreads();
   if (warp == 1) {

@@ -16,7 +16,7 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kStageA = kBM * kBK * 2;             // 16 KiB
 constexpr int kStoreCols = 64;                          // epilogue step: 64 columns
 constexpr uint32_t kStoreBuf = 32u * kStoreCols * 2u;   // 32 rows x 128 B = 4 KiB
-constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 9) + 16u;
+constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 13) + 16u;
 constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
@@ -34,6 +34,7 @@ constexpr int kDetailMmaDrain = (2 << 16) | 3;
 constexpr int kDetailEpiFull = (3 << 16) | 1;
 constexpr int kDetailSkFlag = (3 << 16) | 2;
 constexpr int kDetailSkCopy = (3 << 16) | 3;
+constexpr int kDetailSkFree = (3 << 16) | 4;
 
 struct Params {
   int M, N;              // output extent
@@ -87,6 +88,13 @@ struct Params {
   // first slices come from DRAM; for L2-resident operands the prefetches
   // only delay the ring's own copies).
   int l2_prefetch_first;
+  // 1: every tile is split into two K halves whose walkers form a cluster of
+  // two CTAs (owner = rank 0, contributor = rank 1).  The partial goes
+  // through distributed shared memory instead of the workspace: once the
+  // owner's MMAs are done it tells the contributor that its ring is free,
+  // and the contributor bulk-copies the partial (staged in its own idle
+  // ring) into that ring.
+  int sk_cluster;
   // > 0: the producer also prefetches B into L2, prefetch_kb slices ahead,
   // through a tensor map whose box spans 4 K slices (512 contiguous bytes of
   // each row): memory-bound shapes then read B in longer runs.

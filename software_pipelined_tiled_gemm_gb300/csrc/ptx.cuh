@@ -223,6 +223,18 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Bulk copy from this CTA's shared memory to another CTA's (dst and bar are
+// shared::cluster addresses in the destination CTA); the bytes are counted
+// on the destination's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Arrive on an mbarrier of another CTA in the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
