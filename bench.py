@@ -123,6 +123,98 @@ def traffic_from_profiles(workload, digest):
     return None
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read from NVML (the driver's
+    libnvidia-ml, through ctypes; read-only queries) by a thread every 2 ms,
+    kept only when they fall inside the timed region.  A region of a few tens
+    of milliseconds -- a short bench run -- is too short for nvidia-smi's
+    polling, which then yields one or two samples from outside the load."""
+
+    # nvmlClocksEventReason* bits
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
+                   0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, pci_bus_id, index):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.t0 = self.t1 = None
+
+    def _run(self):
+        ct = self.ct
+        clk, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self.stop_evt.is_set():
+            ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0
+            self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+            self.reasons_fn(self.h, ct.byref(rs))
+            if ok:
+                self.samples.append((time.time(), float(clk.value), mw.value / 1000.0, int(rs.value)))
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread.start()
+        time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        self.stop_evt.set()
+        self.thread.join(timeout=5)
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:
+            pass
+        inside = [x for x in self.samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        window = "timed region"
+        if not inside:
+            if not self.samples:
+                return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"]}
+            mid = (self.t0 + self.t1) / 2 if self.t0 is not None else self.samples[-1][0]
+            inside = sorted(self.samples, key=lambda x: abs(x[0] - mid))[:2]
+            window = "nearest to the timed region"
+        reasons = sorted({n for x in inside for b, n in self.REASON_BITS.items() if x[3] & b})
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(x[2] for x in inside), "source": "nvml"}
+
+
+def make_clock_sampler(dev, index):
+    """NVML sampler when the driver library loads, else nvidia-smi."""
+    try:
+        import torch
+        props = torch.cuda.get_device_properties(dev)
+        bus = None
+        if hasattr(props, "pci_bus_id"):
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                         getattr(props, "pci_device_id", 0))
+        return NvmlClockSampler(bus, index)
+    except Exception:
+        return ClockSampler(index)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples, kept only when they fall inside the
     timed region (host wall-clock window marked with mark_start/mark_stop)."""
@@ -354,7 +446,7 @@ def main():
     # events and a 2 x L2 write runs between steps, outside them.
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = make_clock_sampler(dev, local)
     clocks.start()
     barrier()
     torch.cuda.synchronize(dev)
