@@ -1,0 +1,76 @@
+"""The JSON line bench.py prints: keys, types and internal consistency.
+
+The GPU case runs a short bench of the 4096^3 workload through the library;
+the CPU case runs the reference arm (the fp64 oracle) on the 256^3 workload.
+"""
+from __future__ import annotations
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, timeout=600):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT,
+                         capture_output=True, text=True, timeout=timeout)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [x for x in out.stdout.strip().splitlines() if x.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def _check_common(d, steps, warmup):
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "dtype", "data", "config", "e2e"):
+        assert k in d, k
+    assert d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert d["steps"] == steps and d["warmup"] == warmup and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert isinstance(d["config"], dict) and "workload" in d["config"]
+    assert set(d["e2e"]) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"}
+
+
+@pytest.mark.gpu
+def test_gpu_bench_line_has_the_contract_keys():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    steps, warmup = 5, 3
+    d = _run(["--workload", "gemm_4096_f16", "--steps", str(steps), "--warmup", str(warmup),
+              "--e2e-steps", "2", "--dist-reps", "0", "--cpu-seconds", "1"])
+    _check_common(d, steps, warmup)
+    assert d["scaling"] == "weak" and d["data"].startswith("synthetic")
+    assert d["vs_baseline"] is None or d["vs_baseline"] > 0
+    # roofline of the dominant kernel
+    r = d["roofline"]
+    assert r["bound"] in ("tensor", "hbm") and r["unit"] in ("TFLOP/s", "GB/s")
+    assert 0 < r["frac"] < 1.5 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-6
+    assert r["traffic"] is None or r["traffic"] > 0
+    # one GEMM launch per step (the operands are aligned: no padding copy)
+    assert d["gpu_launches"] == steps
+    # the oracle timed on the host cores
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    # end to end through host buffers: A and B in, C out, every step
+    e = d["e2e"]
+    assert e["h2d_bytes_per_step"] == 2 * 2 * 4096 * 4096
+    assert e["d2h_bytes_per_step"] == 2 * 4096 * 4096
+    assert 0 < e["value"] <= d["value"] * 1.05
+    c = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
+
+
+def test_reference_arm_times_the_oracle_on_cpu():
+    steps, warmup = 1, 1
+    d = _run(["--impl", "reference", "--workload", "gemm_256_f16", "--steps", str(steps),
+              "--warmup", str(warmup)], timeout=300)
+    _check_common(d, steps, warmup)
+    assert d["impl"] == "reference"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
