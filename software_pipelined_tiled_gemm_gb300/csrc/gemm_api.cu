@@ -97,6 +97,10 @@ constexpr int kHostPanelsMax = 4;
 constexpr int64_t kHostPanelMinRows = 1024;
 constexpr size_t kHostPanelMinBytes = 32u << 20;
 
+// Automatic stream-K also needs the last, partial wave to leave each walker
+// idle for at least this many K slices: (1 - leftover tiles / walkers) x K.
+constexpr int kStreamKMinIdleSlices = 24;
+
 struct gemm_plan {
   int device = 0;
   int64_t M = 0, N = 0, K = 0;
@@ -365,8 +369,11 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
 
   // Tile shape.  Candidates in order of preference: CTA pairs (256-row
   // tiles; each CTA holds half of B, so a slot is 32 KiB at tile_n 256 and
-  // deeper rings fit) when at least one full wave of pair tiles exists,
-  // then single-CTA 128-row tiles from the widest down.  A candidate must
+  // deeper rings fit) when at least half a wave of pair tiles exists, then
+  // single-CTA 128-row tiles from the widest down.  Half a wave of 256 x 256
+  // tiles beats one to two waves of 256 x 128 ones, which run at ~72 % of
+  // the wider tiles' rate (2048^3: 20.4 vs 26.5 us; 4096 x 1024 x 8192: 47.7
+  // vs 72.3 us).  A candidate must
   // fit the shared-memory budget; single-CTA widths narrow while the widest
   // leaves most SMs idle (fewer tiles than SMs).
   struct Cand { int cg, bn; };
@@ -388,7 +395,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         cdiv(std::max<int64_t>(M, 1), kBM * cg) * cdiv(std::max<int64_t>(N, 1), bn);
     int clusters = 0;
     if (cg == 2) {
-      // Auto mode takes pairs only for problems with at least a wave of pair tiles.
+      // Auto mode takes pairs only for problems with at least half a wave of pair tiles.
       if (want_cg == 0 && M <= kBM) continue;
       e = set_smem(bn, cg, static_cast<size_t>(smem_optin));
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
@@ -396,7 +403,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
                     : gemm_max_clusters_pair256(need, &clusters);
       if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
       if (clusters < 1) continue;
-      if (want_cg == 0 && tiles < clusters) continue;
+      if (want_cg == 0 && 2 * tiles < clusters) continue;
     }
     chosen = bn;
     chosen_cg = cg;
@@ -508,8 +515,15 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     // Automatic stream-K needs long tiles: exchanging one partial costs about
     // as much as a few K slices, so with short K it loses more than the idle
     // part of the last wave (16896 x 512 x 640: 26 us with, 19 us without).
+    // It must also have idle time to recover: with a nearly full last wave
+    // the exchanges cost more than they save (3072^3, 68 of 76 pair tiles in
+    // the last wave, 5 idle slices per walker: 13 % slower with it; 4096^3,
+    // 40 idle slices: 4 % faster).
     const bool sk_ok = rem > 0 && p->num_tiles >= walkers && sk_fits &&
-                       (want_split == 1 ? k_slots >= 2 : k_blocks >= kStreamKMinKBlocks);
+                       (want_split == 1 ? k_slots >= 2
+                                        : k_blocks >= kStreamKMinKBlocks &&
+                                              (walkers - rem) * k_blocks >=
+                                                  static_cast<int64_t>(kStreamKMinIdleSlices) * walkers);
     const int max_s = std::min(kMaxTailSplits, p->bn / kStoreCols);
     if (want_split == 1 || (want_split == 0 && sk_ok)) {
       if (!sk_ok && want_split == 1 && rem > 0) {

@@ -465,6 +465,27 @@ def test_auto_tail_split_choice():
     p.close()
 
 
+def test_auto_tile_and_stream_k_choice_for_mid_sizes():
+    # Half a wave of 256 x 256 pair tiles is taken over one to two waves of
+    # 256 x 128 ones; stream-K only when the last wave leaves each walker at
+    # least 24 idle K slices.
+    import software_pipelined_tiled_gemm_gb300 as sg
+
+    def info(M, N, K):
+        p = sg.Plan(M, N, K, "f16", stages=6)
+        try:
+            return p.info()
+        finally:
+            p.close()
+
+    for shape in [(2048, 2048, 2048), (4096, 1024, 8192), (512, 8192, 4096)]:
+        i = info(*shape)         # 64 pair tiles on 76 clusters
+        assert i["cta_group"] == 2 and i["tile_n"] == 256 and i["stream_k"] == 0, (shape, i)
+    assert info(3072, 3072, 3072)["stream_k"] == 0    # 68 of 76 in the last wave: 5 idle slices
+    assert info(6144, 6144, 2048)["stream_k"] == 0    # 44 of 76, K = 32 slices: 13.5
+    assert info(4096, 4096, 4096)["stream_k"] == 1    # 28 of 76, K = 64 slices: 40
+
+
 # ------------------------------------------------------------ stream-K --
 
 @pytest.mark.parametrize("cta_group", [1, 2])
