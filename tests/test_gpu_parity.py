@@ -484,6 +484,8 @@ def test_auto_tile_and_stream_k_choice_for_mid_sizes():
     assert info(3072, 3072, 3072)["stream_k"] == 0    # 68 of 76 in the last wave: 5 idle slices
     assert info(6144, 6144, 2048)["stream_k"] == 0    # 44 of 76, K = 32 slices: 13.5
     assert info(4096, 4096, 4096)["stream_k"] == 1    # 28 of 76, K = 64 slices: 40
+    i = info(128, 16384, 2048)      # 128 single-CTA tiles 128 wide keep 84 % of the SMs busy
+    assert i["cta_group"] == 1 and i["tile_n"] == 128, i
 
 
 # ------------------------------------------------------------ stream-K --
