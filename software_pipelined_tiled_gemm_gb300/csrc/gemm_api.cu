@@ -421,7 +421,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         2 * tiles <= prop.multiProcessorCount && 10 * 2 * tiles >= 8 * prop.multiProcessorCount &&
         cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
         static_cast<int64_t>(stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
-            static_cast<int64_t>(kEpiWarps) * 32 * bn * 4)
+            static_cast<int64_t>(epi_cta_partial_bytes(bn)))
       break;
   }
   if (chosen == 0) {
@@ -498,7 +498,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->sk_tiles = 0;
   const int64_t ring_all = static_cast<int64_t>(stages) *
                            (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
-  const bool ring_holds_partial = ring_all >= static_cast<int64_t>(kEpiWarps) * 32 * p->bn * 4;
+  const bool ring_holds_partial = ring_all >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn));
   if (variant == GEMM_PIPELINED && want_split == 0 && chosen_cg == 1 && p->num_tiles > 0 &&
       2 * p->num_tiles <= walkers && k_blocks >= 16 && k_blocks % 2 == 0 && ring_holds_partial) {
     // Few tiles (at most half a wave): split every tile in two equal K halves
@@ -515,7 +515,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     const int64_t rem = p->num_tiles % walkers;
     const int64_t ring = static_cast<int64_t>(stages) *
                          (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
-    const bool sk_fits = ring >= static_cast<int64_t>(kEpiWarps) * 32 * p->bn * 4;
+    const bool sk_fits = ring >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn));
     // Automatic stream-K needs long tiles: exchanging one partial costs about
     // as much as a few K slices, so with short K it loses more than the idle
     // part of the last wave (16896 x 512 x 640: 26 us with, 19 us without).
@@ -534,7 +534,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         delete p;
         return fail(GEMM_ERR_INVALID_ARG,
                     "stream-K needs at least one full wave of tiles and a ring of >= %d B",
-                    kEpiWarps * 32 * p->bn * 4);
+                    static_cast<int>(epi_cta_partial_bytes(p->bn)));
       }
       if (sk_ok) {
         p->dp_tiles = (p->num_tiles / walkers - 1) * walkers;
@@ -606,7 +606,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   }
   if (p->sk_tiles > 0) {
     const size_t nflags = static_cast<size_t>(p->sk_tiles) * chosen_cg * kEpiWarps;
-    if ((e = cudaMalloc(&p->sk_ws, nflags * 32 * p->bn * sizeof(float))) != cudaSuccess ||
+    if ((e = cudaMalloc(&p->sk_ws, nflags * epi_warp_partial_bytes(p->bn))) != cudaSuccess ||
         (e = cudaMalloc(&p->sk_flags, nflags * sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(p->sk_flags, 0, nflags * sizeof(int))) != cudaSuccess) {
       if (p->sk_ws) cudaFree(p->sk_ws);

@@ -21,13 +21,15 @@
 //                       it (the hazard the guide's delay_release covers), and
 //                       the issuer never waits on its own MMAs.  After the
 //                       unit's last slot: commit -> tmem_full[acc].
-//   warps 2-5           epilogue: wait tmem_full[acc]; for stream-K owners,
-//                       add the other walker's fp32 partial; then tcgen05.ld
-//                       32 rows x 64 columns per step, add the bias (if
-//                       any), apply the epilogue function, round, write a
-//                       swizzled staging tile and send it out with a TMA
-//                       store (or row-wise stores when C's pitch is not
-//                       16-byte aligned); then arrive on
+//   warps 2-9           epilogue, two warps per TMEM lane quarter (warp w
+//                       may read lanes 32*(w%4) ..), each taking one half of
+//                       the unit's columns: wait tmem_full[acc]; for
+//                       stream-K owners, add the other walker's fp32 partial;
+//                       then tcgen05.ld 32 rows x 64 columns per step, add
+//                       the bias (if any), apply the epilogue function,
+//                       round, write a swizzled staging tile and send it out
+//                       with a TMA store (or row-wise stores when C's pitch
+//                       is not 16-byte aligned); then arrive on
 //                       tmem_empty[acc].
 //
 // With two TMEM accumulators the epilogue of one unit overlaps the main loop
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSlotA = kStageA * kSub;        // A part of a slot
   constexpr uint32_t kStage = kSlotA + kStageB * kSub;  // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
-  constexpr uint32_t kWarpPartial = 32u * BN * 4u;   // fp32 partial of one epilogue warp
+  constexpr uint32_t kWarpPartial = epi_warp_partial_bytes(BN);  // fp32 partial of one epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B
@@ -352,11 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + a); };
   auto tempty_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + 2 + a); };
   const uint32_t done_bar = bar_base + 8u * (2 * kMaxStages + 4);
-  auto fix_bar = [&](int q) { return bar_base + 8u * (2 * kMaxStages + 5 + q); };
+  auto fix_bar = [&](int e) { return bar_base + 8u * (2 * kMaxStages + 5 + e); };
   // Cluster split: the owner tells the contributor its ring is free.
-  auto free_bar = [&](int q) { return bar_base + 8u * (2 * kMaxStages + 9 + q); };
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes + 8u * (2 * kMaxStages + 13));
+  auto free_bar = [&](int e) { return bar_base + 8u * (2 * kMaxStages + 5 + kEpiWarps + e); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ring_bytes + staging_bytes +
+                                                    8u * (2 * kMaxStages + 5 + 2 * kEpiWarps));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -604,8 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
+    // Warp 2 + e: TMEM lane quarter q (rows q*32 .. q*32+31 of the CTA's
+    // accumulator) and column group g of every unit.  Stream-K partials,
+    // flags and fix-up barriers are per warp e.
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    const int ew = warp - 2;      // owner index of the staging buffers
+    const int ew = warp - 2;      // epilogue warp index: staging, partials, flags
+    const int g = ew / 4;         // column group
     uint8_t* my_stage = staging + ew * p.store_bufs * kStoreBuf;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -620,13 +626,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool narrow = kSplit && x.sub >= 0;
       const int n_width = narrow ? BN / p.tail_splits : BN;
       const int n0 = nb * BN + (narrow ? x.sub * n_width : 0);
-      const uint32_t chunks = static_cast<uint32_t>(n_width) / kStoreCols;
-      // Bias of the first 64-column chunk, fetched before the accumulator
-      // wait so its latency hides there (later chunks: one chunk ahead).
+      // This warp's columns [c_lo, c_hi) of the unit (empty for the second
+      // group of a 64-wide unit); a full-width unit gives every warp
+      // kWarpPartial bytes of partial sum.
+      const int gcols = epi_group_cols(n_width);
+      const int c_lo = g * gcols;
+      const int c_hi = c_lo + gcols < n_width ? c_lo + gcols : n_width;
+      const bool has_cols = c_lo < c_hi;
+      // Bias of the warp's first 64-column chunk, fetched before the
+      // accumulator wait so its latency hides there (later chunks: one chunk
+      // ahead).
       float nb0 = 0.0f, nb1 = 0.0f;
-      if (p.bias != nullptr && x.role != kContrib) {
-        nb0 = load_bias(p, n0 + lane, bf16);
-        nb1 = load_bias(p, n0 + 32 + lane, bf16);
+      if (p.bias != nullptr && x.role != kContrib && has_cols) {
+        nb0 = load_bias(p, n0 + c_lo + lane, bf16);
+        nb1 = load_bias(p, n0 + c_lo + 32 + lane, bf16);
       }
       int ready = 1;
       if (lane == 0) ready = wait_bounded<true>(tfull_bar(acc), acc_phase, p, kDetailEpiFull) ? 1 : 0;
@@ -638,9 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
       // Stream-K: this warp's fp32 partial of a shared tile, laid out
-      // [column][lane] (one coalesced 128-byte line per column).
+      // [column - c_lo][lane] (one coalesced 128-byte line per column).
       const uint32_t flag_idx =
-          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * kEpiWarps + q;
+          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * kEpiWarps + ew;
       float* partial = (kSplit && x.role != kWhole)
                            ? p.sk_ws + static_cast<size_t>(flag_idx) * (kWarpPartial / 4u)
                            : nullptr;
@@ -652,63 +665,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         // owner's fix-up barrier.  Rows >= M are never stored, so their warps
         // exchange nothing.  The final cluster barrier keeps this CTA (the
         // copy's source) alive until the owner has received the bytes.
-        if (row0 < p.M) {
-          float* stage_out = reinterpret_cast<float*>(smem + q * kWarpPartial);
+        if (row0 < p.M && has_cols) {
+          float* stage_out = reinterpret_cast<float*>(smem + ew * kWarpPartial);
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
+          for (int c = c_lo; c < c_hi; c += 32) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(t_row + c, v);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stage_out[(c + j) * 32 + lane] = __uint_as_float(v[j]);
+            for (int j = 0; j < 32; ++j)
+              stage_out[(c - c_lo + j) * 32 + lane] = __uint_as_float(v[j]);
           }
           ptx::fence_proxy_async_smem();  // generic writes -> the copy engine
           __syncwarp();
           int ok = 1;
           if (lane == 0) {
             // A walker holds one unit in this mode, so the barrier's first phase.
-            ok = wait_bounded_cluster<2>(free_bar(q), 0, p, kDetailSkFree) ? 1 : 0;
+            ok = wait_bounded_cluster<2>(free_bar(ew), 0, p, kDetailSkFree) ? 1 : 0;
             if (ok)
-              ptx::bulk_copy_to_peer(ptx::map_shared_rank(sbase + q * kWarpPartial, 0),
-                                     sbase + q * kWarpPartial, kWarpPartial,
-                                     ptx::map_shared_rank(fix_bar(q), 0));
+              ptx::bulk_copy_to_peer(ptx::map_shared_rank(sbase + ew * kWarpPartial, 0),
+                                     sbase + ew * kWarpPartial, kWarpPartial,
+                                     ptx::map_shared_rank(fix_bar(ew), 0));
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
       } else if (kSplit && x.role == kContrib) {
         // Publish the partial sum of K slices [k0, k1) and raise the flag.
+        if (has_cols) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c, v);
-          ptx::tmem_wait_ld();
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(t_row + c, v);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) __stcg(partial + (c + j) * 32 + lane, __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j)
+              __stcg(partial + (c - c_lo + j) * 32 + lane, __uint_as_float(v[j]));
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(p.sk_flags + flag_idx, 1);
         }
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(p.sk_flags + flag_idx, 1);
       } else if (kSplit && x.role == kOwner && p.sk_cluster) {
         // Cluster split: this walker's MMAs are done (accumulator full), so
         // its ring is idle; let the contributor copy its partial there.
-        if (row0 < p.M) {
+        if (row0 < p.M && has_cols) {
           int ok = 1;
           if (lane == 0) {
             // Arm the fix-up barrier for the partial's bytes before telling
             // the contributor that the ring may be written.
-            ptx::mbar_arrive_expect_tx(fix_bar(q), kWarpPartial);
-            ptx::mbar_arrive_cluster(ptx::map_shared_rank(free_bar(q), 1));
-            ok = wait_bounded_cluster<2>(fix_bar(q), fix_phase, p, kDetailSkCopy) ? 1 : 0;
+            ptx::mbar_arrive_expect_tx(fix_bar(ew), kWarpPartial);
+            ptx::mbar_arrive_cluster(ptx::map_shared_rank(free_bar(ew), 1));
+            ok = wait_bounded_cluster<2>(fix_bar(ew), fix_phase, p, kDetailSkCopy) ? 1 : 0;
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           // Every lane acquires the contributor's writes (the phase is complete).
-          (void)ptx::mbar_try_wait_cluster(fix_bar(q), fix_phase);
+          (void)ptx::mbar_try_wait_cluster(fix_bar(ew), fix_phase);
           fix_phase ^= 1u;
           have_partial = true;
         }
-      } else if (kSplit && x.role == kOwner) {
+      } else if (kSplit && x.role == kOwner && has_cols) {
         // The other walker's partial (K slices [k1, k_blocks)) was written at
         // the start of its range.  This is the last unit of this walker, so
         // the ring is idle: bulk-copy the partial into it.
@@ -717,9 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_flag(p.sk_flags + flag_idx, p, kDetailSkFlag) ? 1 : 0;
           if (ok) {
             p.sk_flags[flag_idx] = 0;  // ready for the next launch
-            ptx::mbar_arrive_expect_tx(fix_bar(q), kWarpPartial);
-            ptx::bulk_load(sbase + q * kWarpPartial, partial, kWarpPartial, fix_bar(q));
-            ok = wait_bounded(fix_bar(q), fix_phase, p, kDetailSkCopy) ? 1 : 0;
+            ptx::mbar_arrive_expect_tx(fix_bar(ew), kWarpPartial);
+            ptx::bulk_load(sbase + ew * kWarpPartial, partial, kWarpPartial, fix_bar(ew));
+            ok = wait_bounded(fix_bar(ew), fix_phase, p, kDetailSkCopy) ? 1 : 0;
           }
         }
         fix_phase ^= 1u;
@@ -727,24 +744,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         have_partial = ok != 0;
         if (!have_partial) break;
       }
-      if ((!kSplit || x.role != kContrib) && row0 < p.M) {
-        const float* fix = reinterpret_cast<const float*>(smem + q * kWarpPartial);
+      if ((!kSplit || x.role != kContrib) && row0 < p.M && has_cols) {
+        const float* fix = reinterpret_cast<const float*>(smem + ew * kWarpPartial);
 #pragma unroll 1
-        for (uint32_t c = 0; c < chunks; ++c) {
-          const int col0 = n0 + static_cast<int>(c) * kStoreCols;
+        for (int cc = c_lo; cc < c_hi; cc += kStoreCols) {  // 64-column chunks
+          const int col0 = n0 + cc;
           if (col0 >= p.N) break;
           const float b0 = nb0, b1 = nb1;
-          if (p.bias != nullptr && c + 1 < chunks) {
+          if (p.bias != nullptr && cc + kStoreCols < c_hi) {
             nb0 = load_bias(p, col0 + kStoreCols + lane, bf16);
             nb1 = load_bias(p, col0 + kStoreCols + 32 + lane, bf16);
           }
           uint32_t r0[32], r1[32];
-          ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols, r0);
-          ptx::tmem_ld_32x32b_x32(t_row + c * kStoreCols + 32, r1);
+          ptx::tmem_ld_32x32b_x32(t_row + cc, r0);
+          ptx::tmem_ld_32x32b_x32(t_row + cc + 32, r1);
           ptx::tmem_wait_ld();
           if (kSplit && have_partial) {
             // own slices first, then the partial: a fixed order on every run
-            const int cb = static_cast<int>(c) * kStoreCols;
+            const int cb = cc - c_lo;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               r0[j] = __float_as_uint(__uint_as_float(r0[j]) + fix[(cb + j) * 32 + lane]);

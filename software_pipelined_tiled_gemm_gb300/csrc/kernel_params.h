@@ -10,13 +10,16 @@ namespace spgemm {
 constexpr int kBM = 128;          // CTA tile rows (one TMEM lane per row)
 constexpr int kBK = 64;           // K slice: 64 x 16-bit = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // K of one tcgen05.mma kind::f16
-constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kEpiWarps = 4;
+constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+// Epilogue warps: two per TMEM lane quarter (a warp may read only the quarter
+// warp % 4), each taking one column group of the tile.
+constexpr int kEpiColGroups = 2;
+constexpr int kEpiWarps = 4 * kEpiColGroups;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kStageA = kBM * kBK * 2;             // 16 KiB
 constexpr int kStoreCols = 64;                          // epilogue step: 64 columns
 constexpr uint32_t kStoreBuf = 32u * kStoreCols * 2u;   // 32 rows x 128 B = 4 KiB
-constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 13) + 16u;
+constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 5 + 2 * kEpiWarps) + 16u;
 constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
@@ -120,6 +123,20 @@ struct Params {
   // copies of its first K slice (see gemm_tuning_t::debug_fault).
   int inject_fault;
 };
+
+// Columns of one epilogue column group for a unit `n_width` columns wide:
+// half of it, but whole 64-column store chunks (a 64-wide unit has one group).
+__host__ __device__ constexpr int epi_group_cols(int n_width) {
+  return n_width / kEpiColGroups >= kStoreCols ? n_width / kEpiColGroups : kStoreCols;
+}
+// fp32 partial sum of one epilogue warp (32 rows x its column group) and of
+// a whole CTA (all its epilogue warps) for a full-width tile.
+__host__ __device__ constexpr uint32_t epi_warp_partial_bytes(int bn) {
+  return 32u * static_cast<uint32_t>(epi_group_cols(bn)) * 4u;
+}
+__host__ __device__ constexpr size_t epi_cta_partial_bytes(int bn) {
+  return static_cast<size_t>(kEpiWarps) * epi_warp_partial_bytes(bn);
+}
 
 // Shared memory a CTA needs for a given tile width / ring depth / staging;
 // with a CTA pair (cta_group 2) each CTA holds half of the tile's B rows.
