@@ -124,6 +124,11 @@ typedef struct {
                           the next wave starts on the slices the last one read most
                           recently), -1 = always upwards.  Ignored for a single row of
                           tiles, whose K loops are staggered instead */
+  int epi_groups;      /* epilogue warps: 0 = auto (eight when K is at most 16 slices of 64
+                          or the tiles form a single row, where the epilogue is not hidden
+                          behind the main loop; else four), 1 = four (one per TMEM lane
+                          quarter, two staging buffers each), 2 = eight (two per quarter,
+                          each taking half of a tile's columns) */
 } gemm_tuning_t;
 
 /* Read-only description of what a plan will launch (for tests and benchmarks). */
@@ -157,6 +162,7 @@ typedef struct {
   int sk_cluster;              /* 1: every tile is split into two K halves on the two CTAs
                                   of a cluster, whose partial sum moves through
                                   distributed shared memory */
+  int epi_groups;              /* epilogue column groups: 1 (four warps) or 2 (eight) */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

@@ -62,7 +62,7 @@ class GemmTuning(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("cta_group", ctypes.c_int),
                 ("tail_split", ctypes.c_int), ("timeout_ns", ctypes.c_int64),
                 ("b_kn", ctypes.c_int), ("out_f32", ctypes.c_int), ("debug_fault", ctypes.c_int),
-                ("k_serpentine", ctypes.c_int)]
+                ("k_serpentine", ctypes.c_int), ("epi_groups", ctypes.c_int)]
 
 
 class GemmPlanInfo(ctypes.Structure):
@@ -77,7 +77,7 @@ class GemmPlanInfo(ctypes.Structure):
                 ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int), ("b_kn", ctypes.c_int),
                 ("k_sub", ctypes.c_int), ("host_panels", ctypes.c_int),
                 ("k_serpentine", ctypes.c_int), ("l2_prefetch_first", ctypes.c_int),
-                ("sk_cluster", ctypes.c_int)]
+                ("sk_cluster", ctypes.c_int), ("epi_groups", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -250,7 +250,7 @@ class Plan:
 
     def __init__(self, M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
                  tile_n=0, raster_group=0, max_ctas=0, cta_group=0, tail_split=0,
-                 timeout_ns=0, b_kn=0, out_f32=0, debug_fault=0, k_serpentine=0):
+                 timeout_ns=0, b_kn=0, out_f32=0, debug_fault=0, k_serpentine=0, epi_groups=0):
         self.M, self.N, self.K = int(M), int(N), int(K)
         self.dtype = _DT[dtype] if isinstance(dtype, str) else int(dtype)
         self.epi = _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue)
@@ -260,7 +260,7 @@ class Plan:
         self._h = None
         tuning = GemmTuning(int(tile_n), int(raster_group), int(max_ctas), int(cta_group),
                             int(tail_split), int(timeout_ns), int(b_kn), int(out_f32),
-                            int(debug_fault), int(k_serpentine))
+                            int(debug_fault), int(k_serpentine), int(epi_groups))
         st, h = gemm_plan_create_ex(self.M, self.N, self.K, self.dtype, self.epi, self.stages,
                                     self.variant, self.device, tuning)
         _check(st, "gemm_plan_create")

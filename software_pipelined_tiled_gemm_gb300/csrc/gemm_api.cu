@@ -124,6 +124,7 @@ struct gemm_plan {
   int out_f32 = 0;               // C element: 0 = input type, 1 = fp32
   int b_kn = 0;                  // B stored K x N (read MN-major)
   int k_sub = 1;                 // 64-wide K slices per ring slot
+  int epi_groups = 1;            // epilogue column groups (1: 4 warps, 2: 8 warps)
   int k_serpentine = 0;          // odd waves walk K downwards
   int l2_prefetch_first = 0;     // prefetch the first ring's slices before the PDL wait
   int sk_cluster = 0;            // K halves exchanged within 2-CTA clusters
@@ -343,6 +344,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
       return fail(GEMM_ERR_INVALID_ARG, "out_f32 %d not in {0, 1}", tuning->out_f32);
     if (tuning->b_kn < 0 || tuning->b_kn > 1)
       return fail(GEMM_ERR_INVALID_ARG, "b_kn %d not in {0, 1}", tuning->b_kn);
+    if (tuning->epi_groups < 0 || tuning->epi_groups > 2)
+      return fail(GEMM_ERR_INVALID_ARG, "epi_groups %d not in {0, 1, 2}", tuning->epi_groups);
     if (tuning->k_serpentine < -1 || tuning->k_serpentine > 1)
       return fail(GEMM_ERR_INVALID_ARG, "k_serpentine %d not in {-1, 0, 1}",
                   tuning->k_serpentine);
@@ -378,17 +381,27 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   // leaves most SMs idle (fewer tiles than SMs).
   struct Cand { int cg, bn; };
   const Cand cands[5] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
-  int chosen = 0, chosen_cg = 1, chosen_bufs = 0, chosen_clusters = 0;
+  int chosen = 0, chosen_cg = 1, chosen_bufs = 0, chosen_clusters = 0, chosen_groups = 1;
   size_t chosen_smem = 0;
   for (int i = 0; i < 5; ++i) {
     const int cg = cands[i].cg, bn = cands[i].bn;
     if (want_bn != 0 && bn != want_bn) continue;
     if (want_cg != 0 && cg != want_cg) continue;
+    // Eight epilogue warps where the epilogue is not hidden behind the main
+    // loop: short K, or a single row of tiles (8192 x 8192 x 512: 59.7 ->
+    // 55.3 us; 16896 x 512 x 640 13.3 -> 13.0 us).  Elsewhere four: a second
+    // epilogue warp on the MMA issuer's sub-partition cost 0.9 % of the
+    // cycles at 8192^3.
+    const int groups =
+        (tuning && tuning->epi_groups) ? tuning->epi_groups
+                                       : ((cdiv(K, kBK) <= 16 || cdiv(std::max<int64_t>(M, 1), kBM * cg) == 1)
+                                              ? 2
+                                              : 1);
     int bufs = 2;
-    size_t need = kernel_smem_bytes(bn, stages, bufs, cg);
+    size_t need = kernel_smem_bytes(bn, stages, bufs, cg, groups);
     if (need > static_cast<size_t>(smem_optin)) {
       bufs = 1;
-      need = kernel_smem_bytes(bn, stages, bufs, cg);
+      need = kernel_smem_bytes(bn, stages, bufs, cg, groups);
     }
     if (need > static_cast<size_t>(smem_optin)) continue;
     const int64_t tiles =
@@ -409,6 +422,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     chosen_cg = cg;
     chosen_smem = need;
     chosen_bufs = bufs;
+    chosen_groups = groups;
     chosen_clusters = clusters;
     // Whole tiles that keep at least 80 % of the SMs busy are wide enough:
     // 128 x 16384 x 2048 runs 20.5 us on 128 tiles 128 wide, 26.1 us on 256
@@ -421,7 +435,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         2 * tiles <= prop.multiProcessorCount && 10 * 2 * tiles >= 8 * prop.multiProcessorCount &&
         cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
         static_cast<int64_t>(stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
-            static_cast<int64_t>(epi_cta_partial_bytes(bn)))
+            static_cast<int64_t>(epi_cta_partial_bytes(bn, groups)))
       break;
   }
   if (chosen == 0) {
@@ -452,6 +466,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->cg = chosen_cg;
   p->smem = chosen_smem;
   p->store_bufs = chosen_bufs;
+  p->epi_groups = chosen_groups;
   p->tiles_m = cdiv(M, kBM * chosen_cg);
   p->tiles_n = cdiv(N, chosen);
   p->num_tiles = p->tiles_m * p->tiles_n;
@@ -498,7 +513,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->sk_tiles = 0;
   const int64_t ring_all = static_cast<int64_t>(stages) *
                            (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
-  const bool ring_holds_partial = ring_all >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn));
+  const bool ring_holds_partial =
+      ring_all >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
   if (variant == GEMM_PIPELINED && want_split == 0 && chosen_cg == 1 && p->num_tiles > 0 &&
       2 * p->num_tiles <= walkers && k_blocks >= 16 && k_blocks % 2 == 0 && ring_holds_partial) {
     // Few tiles (at most half a wave): split every tile in two equal K halves
@@ -515,7 +531,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     const int64_t rem = p->num_tiles % walkers;
     const int64_t ring = static_cast<int64_t>(stages) *
                          (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
-    const bool sk_fits = ring >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn));
+    const bool sk_fits = ring >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
     // Automatic stream-K needs long tiles: exchanging one partial costs about
     // as much as a few K slices, so with short K it loses more than the idle
     // part of the last wave (16896 x 512 x 640: 26 us with, 19 us without).
@@ -534,7 +550,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         delete p;
         return fail(GEMM_ERR_INVALID_ARG,
                     "stream-K needs at least one full wave of tiles and a ring of >= %d B",
-                    static_cast<int>(epi_cta_partial_bytes(p->bn)));
+                    static_cast<int>(epi_cta_partial_bytes(p->bn, p->epi_groups)));
       }
       if (sk_ok) {
         p->dp_tiles = (p->num_tiles / walkers - 1) * walkers;
@@ -605,8 +621,9 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
   }
   if (p->sk_tiles > 0) {
-    const size_t nflags = static_cast<size_t>(p->sk_tiles) * chosen_cg * kEpiWarps;
-    if ((e = cudaMalloc(&p->sk_ws, nflags * epi_warp_partial_bytes(p->bn))) != cudaSuccess ||
+    const size_t nflags = static_cast<size_t>(p->sk_tiles) * chosen_cg * 4 * p->epi_groups;
+    if ((e = cudaMalloc(&p->sk_ws, nflags * epi_warp_partial_bytes(p->bn, p->epi_groups))) !=
+            cudaSuccess ||
         (e = cudaMalloc(&p->sk_flags, nflags * sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(p->sk_flags, 0, nflags * sizeof(int))) != cudaSuccess) {
       if (p->sk_ws) cudaFree(p->sk_ws);
@@ -840,6 +857,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.tmem_cols = pow2;
   prm.raster_group = plan->raster_group;
   prm.store_bufs = plan->store_bufs;
+  prm.epi_groups = plan->epi_groups;
   prm.bf16 = plan->dtype == GEMM_BF16 ? 1 : 0;
   prm.epilogue = static_cast<int>(plan->epi);
   prm.out_f32 = plan->out_f32;
@@ -1044,7 +1062,8 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
   if (h[0] != 0 && plan->sk_flags) {
     // A launch that gave up part-way may have left partial-ready flags raised.
     e = cudaMemset(plan->sk_flags, 0,
-                   static_cast<size_t>(plan->sk_tiles) * plan->cg * kEpiWarps * sizeof(int));
+                   static_cast<size_t>(plan->sk_tiles) * plan->cg * 4 * plan->epi_groups *
+                       sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clear stream-K flags");
   }
   *device_status = h[0];
@@ -1080,6 +1099,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->kernels_per_run = plan->last_kernels;
   info->sm_count = plan->sm_count;
   info->k_serpentine = plan->k_serpentine;
+  info->epi_groups = plan->epi_groups;
   info->l2_prefetch_first = plan->l2_prefetch_first;
   info->sk_cluster = plan->sk_cluster;
   info->cta_group = plan->cg;

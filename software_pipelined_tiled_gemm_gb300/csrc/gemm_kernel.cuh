@@ -322,8 +322,13 @@ __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params
 // kSub: 64-wide K slices per ring slot.  With 2, one full/empty barrier
 // round trip covers 8 MMAs instead of 4 (the slot holds two slices of A and
 // two of B side by side); p.stages and p.k_blocks count slots.
-template <int BN, int CG, bool kSplit, bool kKN, bool kStream, int kSub>
-__global__ void __launch_bounds__(kThreads, 1)
+// kEpiG: epilogue column groups, 1 (warps 2-5, 192 threads) or 2 (warps 2-9,
+// 320 threads: two warps per TMEM lane quarter, each taking half of a unit's
+// columns).  Eight warps halve an exposed epilogue; where the epilogue hides
+// behind a long main loop, four run faster (a second epilogue warp on the
+// MMA issuer's sub-partition costs ~0.5-1 % of the cycles at 8192^3).
+template <int BN, int CG, bool kSplit, bool kKN, bool kStream, int kSub, int kEpiG>
+__global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmBp, const Params p) {
@@ -335,7 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSlotA = kStageA * kSub;        // A part of a slot
   constexpr uint32_t kStage = kSlotA + kStageB * kSub;  // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
-  constexpr uint32_t kWarpPartial = epi_warp_partial_bytes(BN);  // fp32 partial of one epilogue warp
+  static_assert(kEpiG == 1 || kEpiG == 2, "one or two epilogue column groups");
+  constexpr int epi_groups = kEpiG;  // epilogue column groups (4 x kEpiG epilogue warps)
+  // fp32 partial of one epilogue warp (32 rows x its column group)
+  const uint32_t warp_partial = epi_warp_partial_bytes(BN, epi_groups);
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.stages;
   const uint32_t ring_bytes = static_cast<uint32_t>(S) * kStage;
   uint8_t* staging = smem + ring_bytes;
-  const uint32_t staging_bytes = kEpiWarps * p.store_bufs * kStoreBuf;
+  const uint32_t staging_bytes = 4u * epi_groups * p.store_bufs * kStoreBuf;
   const uint32_t bar_base = sbase + ring_bytes + staging_bytes;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
       // Every epilogue warp of every CTA of the tile releases the accumulator.
-      ptx::mbar_init(tempty_bar(a), kEpiWarps * CG);
+      ptx::mbar_init(tempty_bar(a), 4 * kEpiG * CG);
     }
     ptx::mbar_init(done_bar, 1);
     for (int q = 0; q < kEpiWarps; ++q) {
@@ -607,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------- epilogue --
     // Warp 2 + e: TMEM lane quarter q (rows q*32 .. q*32+31 of the CTA's
-    // accumulator) and column group g of every unit.  Stream-K partials,
-    // flags and fix-up barriers are per warp e.
+    // accumulator) and column group g = e / 4 of every unit.  Stream-K
+    // partials, flags and fix-up barriers are per warp e.
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int ew = warp - 2;      // epilogue warp index: staging, partials, flags
     const int g = ew / 4;         // column group
@@ -626,13 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool narrow = kSplit && x.sub >= 0;
       const int n_width = narrow ? BN / p.tail_splits : BN;
       const int n0 = nb * BN + (narrow ? x.sub * n_width : 0);
-      // This warp's columns [c_lo, c_hi) of the unit (empty for the second
-      // group of a 64-wide unit); a full-width unit gives every warp
-      // kWarpPartial bytes of partial sum.
-      const int gcols = epi_group_cols(n_width);
+      // This warp's columns [c_lo, c_hi) of the unit (empty for a group not
+      // in use and for the second group of a 64-wide unit); a full-width
+      // unit gives every active warp warp_partial bytes of partial sum.
+      const int gcols = epi_group_cols(n_width, epi_groups);
       const int c_lo = g * gcols;
       const int c_hi = c_lo + gcols < n_width ? c_lo + gcols : n_width;
-      const bool has_cols = c_lo < c_hi;
+      const bool has_cols = g < epi_groups && c_lo < c_hi;
       // Bias of the warp's first 64-column chunk, fetched before the
       // accumulator wait so its latency hides there (later chunks: one chunk
       // ahead).
@@ -653,9 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Stream-K: this warp's fp32 partial of a shared tile, laid out
       // [column - c_lo][lane] (one coalesced 128-byte line per column).
       const uint32_t flag_idx =
-          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * kEpiWarps + ew;
+          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * (4u * epi_groups) + ew;
       float* partial = (kSplit && x.role != kWhole)
-                           ? p.sk_ws + static_cast<size_t>(flag_idx) * (kWarpPartial / 4u)
+                           ? p.sk_ws + static_cast<size_t>(flag_idx) * (warp_partial / 4u)
                            : nullptr;
       bool have_partial = false;
       if (kSplit && x.role == kContrib && p.sk_cluster) {
@@ -666,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exchange nothing.  The final cluster barrier keeps this CTA (the
         // copy's source) alive until the owner has received the bytes.
         if (row0 < p.M && has_cols) {
-          float* stage_out = reinterpret_cast<float*>(smem + ew * kWarpPartial);
+          float* stage_out = reinterpret_cast<float*>(smem + ew * warp_partial);
 #pragma unroll 1
           for (int c = c_lo; c < c_hi; c += 32) {
             uint32_t v[32];
@@ -683,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A walker holds one unit in this mode, so the barrier's first phase.
             ok = wait_bounded_cluster<2>(free_bar(ew), 0, p, kDetailSkFree) ? 1 : 0;
             if (ok)
-              ptx::bulk_copy_to_peer(ptx::map_shared_rank(sbase + ew * kWarpPartial, 0),
-                                     sbase + ew * kWarpPartial, kWarpPartial,
+              ptx::bulk_copy_to_peer(ptx::map_shared_rank(sbase + ew * warp_partial, 0),
+                                     sbase + ew * warp_partial, warp_partial,
                                      ptx::map_shared_rank(fix_bar(ew), 0));
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -714,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             // Arm the fix-up barrier for the partial's bytes before telling
             // the contributor that the ring may be written.
-            ptx::mbar_arrive_expect_tx(fix_bar(ew), kWarpPartial);
+            ptx::mbar_arrive_expect_tx(fix_bar(ew), warp_partial);
             ptx::mbar_arrive_cluster(ptx::map_shared_rank(free_bar(ew), 1));
             ok = wait_bounded_cluster<2>(fix_bar(ew), fix_phase, p, kDetailSkCopy) ? 1 : 0;
           }
@@ -734,8 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_flag(p.sk_flags + flag_idx, p, kDetailSkFlag) ? 1 : 0;
           if (ok) {
             p.sk_flags[flag_idx] = 0;  // ready for the next launch
-            ptx::mbar_arrive_expect_tx(fix_bar(ew), kWarpPartial);
-            ptx::bulk_load(sbase + ew * kWarpPartial, partial, kWarpPartial, fix_bar(ew));
+            ptx::mbar_arrive_expect_tx(fix_bar(ew), warp_partial);
+            ptx::bulk_load(sbase + ew * warp_partial, partial, warp_partial, fix_bar(ew));
             ok = wait_bounded(fix_bar(ew), fix_phase, p, kDetailSkCopy) ? 1 : 0;
           }
         }
@@ -745,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!have_partial) break;
       }
       if ((!kSplit || x.role != kContrib) && row0 < p.M && has_cols) {
-        const float* fix = reinterpret_cast<const float*>(smem + ew * kWarpPartial);
+        const float* fix = reinterpret_cast<const float*>(smem + ew * warp_partial);
 #pragma unroll 1
         for (int cc = c_lo; cc < c_hi; cc += kStoreCols) {  // 64-column chunks
           const int col0 = n0 + cc;

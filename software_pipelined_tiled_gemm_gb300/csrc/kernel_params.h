@@ -10,11 +10,13 @@ namespace spgemm {
 constexpr int kBM = 128;          // CTA tile rows (one TMEM lane per row)
 constexpr int kBK = 64;           // K slice: 64 x 16-bit = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // K of one tcgen05.mma kind::f16
-constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
-// Epilogue warps: two per TMEM lane quarter (a warp may read only the quarter
-// warp % 4), each taking one column group of the tile.
-constexpr int kEpiColGroups = 2;
-constexpr int kEpiWarps = 4 * kEpiColGroups;
+// Epilogue warps: one or two per TMEM lane quarter (a warp may read only the
+// quarter warp % 4), each taking one column group of the tile; a kernel
+// instance has one group (warps 2-5) or two (warps 2-9), Params::epi_groups.
+constexpr int kEpiColGroups = 2;                 // at most
+constexpr int kEpiWarps = 4 * kEpiColGroups;     // at most
+// Threads of a CTA: warp 0 TMA producer, warp 1 MMA issuer, 4 x groups epilogue.
+__host__ __device__ constexpr int kernel_threads(int epi_groups) { return 64 + 128 * epi_groups; }
 constexpr int kMaxStages = 8;
 constexpr uint32_t kStageA = kBM * kBK * 2;             // 16 KiB
 constexpr int kStoreCols = 64;                          // epilogue step: 64 columns
@@ -49,7 +51,8 @@ struct Params {
   int num_acc;           // TMEM accumulators, 1 or 2
   int tmem_cols;         // allocated TMEM columns (power of two >= 32)
   int raster_group;      // tile rows per raster group
-  int store_bufs;        // staging buffers per epilogue warp (1 or 2)
+  int store_bufs;        // staging buffers per active epilogue warp (1 or 2)
+  int epi_groups;        // epilogue column groups: 1 (warps 2-5) or 2 (warps 2-9)
   int bf16;              // element type: 0 fp16, 1 bf16
   int epilogue;          // 0 none, 1 tanh-GELU, 2 ReLU
   int out_f32;           // C element type: 0 = the input type, 1 = fp32
@@ -125,26 +128,30 @@ struct Params {
 };
 
 // Columns of one epilogue column group for a unit `n_width` columns wide:
-// half of it, but whole 64-column store chunks (a 64-wide unit has one group).
-__host__ __device__ constexpr int epi_group_cols(int n_width) {
-  return n_width / kEpiColGroups >= kStoreCols ? n_width / kEpiColGroups : kStoreCols;
+// all of it with one group; with two, half of it, but whole 64-column store
+// chunks (a 64-wide unit then has one non-empty group).
+__host__ __device__ constexpr int epi_group_cols(int n_width, int groups) {
+  return groups < 2 ? n_width
+                    : (n_width / 2 >= kStoreCols ? n_width / 2 : kStoreCols);
 }
 // fp32 partial sum of one epilogue warp (32 rows x its column group) and of
-// a whole CTA (all its epilogue warps) for a full-width tile.
-__host__ __device__ constexpr uint32_t epi_warp_partial_bytes(int bn) {
-  return 32u * static_cast<uint32_t>(epi_group_cols(bn)) * 4u;
+// a whole CTA (all its active epilogue warps) for a full-width tile.
+__host__ __device__ constexpr uint32_t epi_warp_partial_bytes(int bn, int groups) {
+  return 32u * static_cast<uint32_t>(epi_group_cols(bn, groups)) * 4u;
 }
-__host__ __device__ constexpr size_t epi_cta_partial_bytes(int bn) {
-  return static_cast<size_t>(kEpiWarps) * epi_warp_partial_bytes(bn);
+__host__ __device__ constexpr size_t epi_cta_partial_bytes(int bn, int groups) {
+  return static_cast<size_t>(4 * (groups < 2 ? 1 : 2)) * epi_warp_partial_bytes(bn, groups);
 }
 
-// Shared memory a CTA needs for a given tile width / ring depth / staging;
+// Shared memory a CTA needs for a given tile width / ring depth / staging
+// (store_bufs buffers for each of the epi_groups x 4 active epilogue warps);
 // with a CTA pair (cta_group 2) each CTA holds half of the tile's B rows.
-inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs, int cta_group = 1) {
+inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs, int cta_group = 1,
+                                int epi_groups = 1) {
   const size_t stage =
       static_cast<size_t>(kStageA) + static_cast<size_t>(bn / cta_group) * kBK * 2;
   return kAlignSlack + stage * static_cast<size_t>(stages) +
-         static_cast<size_t>(kEpiWarps) * store_bufs * kStoreBuf + kBarrierBytes;
+         static_cast<size_t>(4 * epi_groups) * store_bufs * kStoreBuf + kBarrierBytes;
 }
 
 }  // namespace spgemm

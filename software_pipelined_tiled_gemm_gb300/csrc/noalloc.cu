@@ -214,6 +214,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   p.tmem_cols = std::max(32, bn * 2);
   p.raster_group = static_cast<int>(std::min<int64_t>(16, tm));
   p.store_bufs = bufs;
+  p.epi_groups = 1;
   p.bf16 = dtype == GEMM_BF16 ? 1 : 0;
   p.epilogue = static_cast<int>(epi);
   p.out_f32 = 0;

@@ -79,7 +79,8 @@ def test_plan_create_ex_rejects_bad_tuning():
               sg.GemmTuning(0, 0, 0, 0, 5, 0), sg.GemmTuning(0, 0, 0, 0, 0, -5),
               sg.GemmTuning(0, 0, 0, 0, 0, 0, 2), sg.GemmTuning(b_kn=-1),
               sg.GemmTuning(out_f32=3), sg.GemmTuning(tail_split=2, b_kn=1),
-              sg.GemmTuning(k_serpentine=2), sg.GemmTuning(k_serpentine=-2)):
+              sg.GemmTuning(k_serpentine=2), sg.GemmTuning(k_serpentine=-2),
+              sg.GemmTuning(epi_groups=3), sg.GemmTuning(epi_groups=-1)):
         st, h = sg.gemm_plan_create_ex(64, 64, 64, 0, 0, 4, 0, 0, t)
         assert st == sg.GEMM_ERR_INVALID_ARG and h is None
 
