@@ -21,9 +21,10 @@
 //                       it (the hazard the guide's delay_release covers), and
 //                       the issuer never waits on its own MMAs.  After the
 //                       unit's last slot: commit -> tmem_full[acc].
-//   warps 2-9           epilogue, two warps per TMEM lane quarter (warp w
-//                       may read lanes 32*(w%4) ..), each taking one half of
-//                       the unit's columns: wait tmem_full[acc]; for
+//   warps 2-5 (or 2-9)  epilogue, one (or two) warps per TMEM lane quarter
+//                       (warp w may read lanes 32*(w%4) ..), each taking the
+//                       unit's columns (or one half of them): wait
+//                       tmem_full[acc]; for
 //                       stream-K owners, add the other walker's fp32 partial;
 //                       then tcgen05.ld 32 rows x 64 columns per step, add
 //                       the bias (if any), apply the epilogue function,
@@ -38,8 +39,13 @@
 // and the even CTA issues the MMAs for both.  The CTAs (or pairs) are
 // persistent walkers over a grouped ("rasterised") tile order that keeps
 // `raster_group` tile rows together, so concurrently running walkers share A
-// and B rows in L2; the last, partial wave is shared out stream-K (or cut
-// into narrow tiles).
+// and B rows in L2; with serpentine K, alternate waves walk K downwards so
+// that each starts on the slices its predecessor read last.  The last,
+// partial wave is shared out stream-K (or cut into narrow tiles); a problem
+// of few tiles splits each in two K halves on the two CTAs of a cluster,
+// whose partial moves through distributed shared memory.  Operands larger
+// than L2 have each CTA's first ring prefetched into L2 while the previous
+// kernel in the stream finishes.
 //
 // Every wait is bounded by a wall-clock limit; a wait that runs out records
 // GEMM_ERR_TIMEOUT in the status word and its role stops, after which the CTA
