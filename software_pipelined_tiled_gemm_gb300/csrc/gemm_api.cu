@@ -106,7 +106,8 @@ struct gemm_plan {
   int64_t M = 0, N = 0, K = 0;
   gemm_dtype_t dtype = GEMM_F16;
   gemm_epilogue_t epi = GEMM_EPI_NONE;
-  int stages = 0;
+  int stages = 0;                // as requested (runs must pass the same value)
+  int ring_stages = 0;           // K slices in flight actually built (<= stages)
   gemm_variant_t variant = GEMM_PIPELINED;
 
   int sm_count = 0;
@@ -379,6 +380,15 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   // vs 72.3 us).  A candidate must
   // fit the shared-memory budget; single-CTA widths narrow while the widest
   // leaves most SMs idle (fewer tiles than SMs).
+  // Ring depth actually built: a pipelined plan whose K has fewer slices than
+  // `stages` (and too few for any K split) gets one slot per slice; the
+  // extra slots would only take shared memory (256^3, 4 slices: 8.2 us with
+  // 4 slots against 9.8 us with 6, L2 flushed).
+  const int64_t k_slices = cdiv(K, kBK);
+  const int ring_stages =
+      (variant == GEMM_PIPELINED && want_split == 0 && k_slices >= 1 && k_slices < 16)
+          ? static_cast<int>(std::min<int64_t>(stages, k_slices))
+          : stages;
   struct Cand { int cg, bn; };
   const Cand cands[5] = {{2, 256}, {2, 128}, {1, 256}, {1, 128}, {1, 64}};
   int chosen = 0, chosen_cg = 1, chosen_bufs = 0, chosen_clusters = 0, chosen_groups = 1;
@@ -398,10 +408,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
                                               ? 2
                                               : 1);
     int bufs = 2;
-    size_t need = kernel_smem_bytes(bn, stages, bufs, cg, groups);
+    size_t need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
     if (need > static_cast<size_t>(smem_optin)) {
       bufs = 1;
-      need = kernel_smem_bytes(bn, stages, bufs, cg, groups);
+      need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
     }
     if (need > static_cast<size_t>(smem_optin)) continue;
     const int64_t tiles =
@@ -434,7 +444,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     if (cg == 1 && variant == GEMM_PIPELINED && want_split != -1 &&
         2 * tiles <= prop.multiProcessorCount && 10 * 2 * tiles >= 8 * prop.multiProcessorCount &&
         cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
-        static_cast<int64_t>(stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
+        static_cast<int64_t>(ring_stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
             static_cast<int64_t>(epi_cta_partial_bytes(bn, groups)))
       break;
   }
@@ -454,6 +464,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->dtype = dtype;
   p->epi = epi;
   p->stages = stages;
+  p->ring_stages = ring_stages;
   p->variant = variant;
   p->sm_count = prop.multiProcessorCount;
   p->timeout_ns = timeout;
@@ -504,14 +515,14 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   // 256-byte runs (+8-21 % on 64-128-row problems).  Two slots (4 slices)
   // are too shallow: 8192^3 drops from 1647 to 1498 TFLOP/s.
   p->k_sub = ((chosen_cg == 2 || p->tiles_m == 1) && variant == GEMM_PIPELINED &&
-              stages % 2 == 0 && stages >= 6 && k_blocks >= 4)
+              ring_stages % 2 == 0 && ring_stages >= 6 && k_blocks >= 4)
                  ? 2
                  : 1;
   const int64_t k_slots = cdiv(K, kBK * p->k_sub);
   p->dp_tiles = p->num_tiles;
   p->tail_splits = 1;
   p->sk_tiles = 0;
-  const int64_t ring_all = static_cast<int64_t>(stages) *
+  const int64_t ring_all = static_cast<int64_t>(ring_stages) *
                            (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
   const bool ring_holds_partial =
       ring_all >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
@@ -529,7 +540,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     p->sk_cluster = 1;
   } else if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
     const int64_t rem = p->num_tiles % walkers;
-    const int64_t ring = static_cast<int64_t>(stages) *
+    const int64_t ring = static_cast<int64_t>(ring_stages) *
                          (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
     const bool sk_fits = ring >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
     // Automatic stream-K needs long tiles: exchanging one partial costs about
@@ -848,7 +859,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.tiles_n = static_cast<int>(plan->tiles_n);
   prm.num_tiles = static_cast<int>(plan->num_tiles);
   prm.k_blocks = static_cast<int>(cdiv(Keff, kBK * plan->k_sub));
-  prm.stages = plan->stages / plan->k_sub;
+  prm.stages = plan->ring_stages / plan->k_sub;
   prm.k_sub = plan->k_sub;
   prm.num_acc = plan->num_acc;
   int cols = plan->bn * plan->num_acc;
@@ -1088,7 +1099,7 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->tile_m = kBM * plan->cg;
   info->tile_n = plan->bn;
   info->tile_k = kBK;
-  info->stages = plan->stages;
+  info->stages = plan->ring_stages;
   info->accumulators = plan->num_acc;
   info->raster_group = plan->raster_group;
   info->grid = plan->grid;

@@ -465,6 +465,22 @@ def test_auto_tail_split_choice():
     p.close()
 
 
+def test_ring_depth_capped_at_the_k_slices_of_short_problems():
+    # a ring deeper than K has slices only takes shared memory; runs still
+    # pass the requested stages
+    import software_pipelined_tiled_gemm_gb300 as sg
+    A, B = _int_inputs(256, 256, 256, "f16", seed=1900)          # 4 K slices
+    C, info, canary = gu.run_device(A, B, "f16", stages=6)
+    assert canary and info["stages"] == 4, info
+    _assert_bit_exact(A, B, "f16", C)
+    p = sg.Plan(256, 256, 256, "f16", stages=6, tail_split=-1)   # a forced tail mode keeps the ring
+    assert p.info()["stages"] == 6
+    p.close()
+    p = sg.Plan(512, 512, 2048, "f16", stages=6)                 # 32 slices: not capped
+    assert p.info()["stages"] == 6
+    p.close()
+
+
 def test_auto_tile_and_stream_k_choice_for_mid_sizes():
     # Half a wave of 256 x 256 pair tiles is taken over one to two waves of
     # 256 x 128 ones; stream-K only when the last wave leaves each walker at
