@@ -223,11 +223,25 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
                             int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                             gemm_epilogue_t epi, int stages, void* stream);
 
+/* Where a device-side wait ran out of time (the detail of GEMM_ERR_TIMEOUT):
+ * role << 16 | wait id, role 1 = TMA producer, 2 = MMA issuer, 3 = epilogue. */
+typedef enum {
+  GEMM_WAIT_PRODUCER_EMPTY = (1 << 16) | 1, /* producer: a ring slot to become free */
+  GEMM_WAIT_PRODUCER_DRAIN = (1 << 16) | 2, /* producer: its last copies to land */
+  GEMM_WAIT_MMA_ACC_EMPTY = (2 << 16) | 1,  /* MMA issuer: the epilogue to free an accumulator */
+  GEMM_WAIT_MMA_FULL = (2 << 16) | 2,       /* MMA issuer: a ring slot's copies */
+  GEMM_WAIT_MMA_DRAIN = (2 << 16) | 3,      /* MMA issuer: its last MMAs to complete */
+  GEMM_WAIT_EPI_FULL = (3 << 16) | 1,       /* epilogue: an accumulator to be filled */
+  GEMM_WAIT_SK_FLAG = (3 << 16) | 2,        /* stream-K owner: the partner's partial */
+  GEMM_WAIT_SK_COPY = (3 << 16) | 3,        /* stream-K owner: the partial's bytes */
+  GEMM_WAIT_SK_FREE = (3 << 16) | 4         /* cluster split: the owner's ring to be free */
+} gemm_wait_t;
+
 /* Synchronise the plan's device and read (then clear) its device status word.
  * *device_status receives GEMM_OK or the code a kernel recorded (e.g.
  * GEMM_ERR_TIMEOUT); *detail (may be NULL) receives the place it was recorded
- * (role << 16 | wait id).  Returns GEMM_ERR_CUDA if the synchronisation
- * itself failed. */
+ * (a gemm_wait_t, 0 with no error).  Returns GEMM_ERR_CUDA if the
+ * synchronisation itself failed. */
 gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t* detail);
 
 /* Describe the plan's launch configuration. */
@@ -239,6 +253,10 @@ void gemm_plan_destroy(gemm_plan_t* plan);
 
 /* Static text for a status code ("GEMM_OK", ...). */
 const char* gemm_status_string(gemm_status_t s);
+
+/* Static text for the detail of a device status word ("MMA issuer waiting
+ * for a ring slot's copies", ...); "" for 0, "unknown wait" otherwise. */
+const char* gemm_wait_detail_string(int32_t detail);
 
 /* Last error message recorded by this host thread (argument that failed,
  * CUDA error text), or "" if none.  The pointer stays valid until the next

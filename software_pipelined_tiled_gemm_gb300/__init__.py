@@ -134,6 +134,8 @@ def load_library(path: Optional[str] = None):
         lib.gemm_plan_destroy.restype = None
         lib.gemm_status_string.argtypes = [ci]
         lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_wait_detail_string.argtypes = [ctypes.c_int32]
+        lib.gemm_wait_detail_string.restype = ctypes.c_char_p
         lib.gemm_last_error.argtypes = []
         lib.gemm_last_error.restype = ctypes.c_char_p
         lib.gemm_smem_bytes.argtypes = [ci, ci, ci, ci, ci]
@@ -162,6 +164,11 @@ def _check(status: int, where: str):
 
 def gemm_status_string(status: int) -> str:
     return load_library().gemm_status_string(int(status)).decode()
+
+
+def gemm_wait_detail_string(detail: int) -> str:
+    """Which device-side wait ran out of time, from a device status detail."""
+    return load_library().gemm_wait_detail_string(int(detail)).decode()
 
 
 def gemm_last_error() -> str:

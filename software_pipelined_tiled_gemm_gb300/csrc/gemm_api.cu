@@ -294,6 +294,30 @@ const char* gemm_status_string(gemm_status_t s) {
   return "GEMM_ERR_UNKNOWN";
 }
 
+static_assert(GEMM_WAIT_PRODUCER_EMPTY == kDetailProducerEmpty &&
+                  GEMM_WAIT_PRODUCER_DRAIN == kDetailProducerDrain &&
+                  GEMM_WAIT_MMA_ACC_EMPTY == kDetailMmaAccEmpty && GEMM_WAIT_MMA_FULL == kDetailMmaFull &&
+                  GEMM_WAIT_MMA_DRAIN == kDetailMmaDrain && GEMM_WAIT_EPI_FULL == kDetailEpiFull &&
+                  GEMM_WAIT_SK_FLAG == kDetailSkFlag && GEMM_WAIT_SK_COPY == kDetailSkCopy &&
+                  GEMM_WAIT_SK_FREE == kDetailSkFree,
+              "gemm_wait_t must match the kernel's wait identifiers");
+
+const char* gemm_wait_detail_string(int32_t detail) {
+  switch (detail) {
+    case 0: return "";
+    case GEMM_WAIT_PRODUCER_EMPTY: return "TMA producer waiting for a free ring slot";
+    case GEMM_WAIT_PRODUCER_DRAIN: return "TMA producer waiting for its last copies to land";
+    case GEMM_WAIT_MMA_ACC_EMPTY: return "MMA issuer waiting for the epilogue to free an accumulator";
+    case GEMM_WAIT_MMA_FULL: return "MMA issuer waiting for a ring slot's copies";
+    case GEMM_WAIT_MMA_DRAIN: return "MMA issuer waiting for its last MMAs to complete";
+    case GEMM_WAIT_EPI_FULL: return "epilogue waiting for an accumulator to be filled";
+    case GEMM_WAIT_SK_FLAG: return "stream-K owner waiting for its partner's partial";
+    case GEMM_WAIT_SK_COPY: return "stream-K owner waiting for the partial's bytes";
+    case GEMM_WAIT_SK_FREE: return "cluster split contributor waiting for the owner's ring";
+  }
+  return "unknown wait";
+}
+
 const char* gemm_last_error(void) { return g_last_error.c_str(); }
 
 const char* gemm_version(void) { return "0.1.0"; }

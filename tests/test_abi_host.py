@@ -42,6 +42,21 @@ def test_status_strings():
     assert re.match(r"^\d+\.\d+\.\d+$", sg.gemm_version())
 
 
+def test_wait_detail_strings_name_every_device_wait():
+    # role << 16 | wait id, as the kernels record them under GEMM_ERR_TIMEOUT
+    codes = {(1 << 16) | 1: "producer", (1 << 16) | 2: "producer", (2 << 16) | 1: "MMA",
+             (2 << 16) | 2: "MMA", (2 << 16) | 3: "MMA", (3 << 16) | 1: "epilogue",
+             (3 << 16) | 2: "stream-K", (3 << 16) | 3: "stream-K", (3 << 16) | 4: "cluster"}
+    texts = set()
+    for code, word in codes.items():
+        t = sg.gemm_wait_detail_string(code)
+        assert word in t, (hex(code), t)
+        texts.add(t)
+    assert len(texts) == len(codes)          # each wait has its own text
+    assert sg.gemm_wait_detail_string(0) == ""
+    assert sg.gemm_wait_detail_string(12345) == "unknown wait"
+
+
 def test_smem_bytes_is_the_tutorial_formula():
     # shared_bytes(block_M, block_N, block_K, elem, stages) of the TileLang
     # tutorial: stages * (bM*bK + bN*bK) * elem.  Its CLI defaults (128, 128,

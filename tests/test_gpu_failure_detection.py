@@ -47,6 +47,7 @@ def test_wait_timeout_is_reported_and_context_survives(cta_group):
     plan.close()
     assert status == sg.GEMM_ERR_TIMEOUT, (status, hex(detail))
     assert (detail >> 16) in (1, 2, 3)      # producer, MMA issuer or epilogue
+    assert sg.gemm_wait_detail_string(detail) not in ("", "unknown wait")
     assert elapsed < 10.0
     # The context is still usable and the status word was cleared.
     C, info, canary = gu.run_device(A, B, "f16", cta_group=cta_group, tile_n=256)
