@@ -2,7 +2,8 @@
 
 Each case draws M, N, K (1 .. ~700), the dtype, the epilogue, the B layout,
 the CTA group, the ring depth, the last-wave scheme, fp32 output and
-unaligned operand bases (every third case also adds a per-column bias),
+unaligned operand bases (every third case also adds a per-column bias; the
+epilogue-warp count and the serpentine K order cycle with the case number),
 runs the CUDA path through the C ABI and compares
 every element with the fp64 oracle (2 ulp + 1e-3 per element, relative
 Frobenius 1e-3).  Option combinations the planner rejects by design (for
@@ -56,13 +57,15 @@ def _draw(rng):
     }
 
 
-def _run_case(cfg, with_bias=False):
+def _run_case(cfg, with_bias=False, epi_groups=0, k_serpentine=0):
     import software_pipelined_tiled_gemm_gb300 as sg
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     dtype, epi = cfg["dtype"], cfg["epilogue"]
     A, B = gemm_inputs.custom(M, N, K, dtype=dtype, dist="normal_scaled",
                               seed=M * 7919 + N * 31 + K)
     tuning = {k: cfg[k] for k in ("b_kn", "cta_group", "tail_split", "out_f32", "max_ctas")}
+    tuning["epi_groups"] = epi_groups
+    tuning["k_serpentine"] = k_serpentine
     if tuning["cta_group"] == 2:
         tuning["tile_n"] = 256 if cfg["stages"] <= 6 else 128
     dev = torch.device("cuda", 0)
@@ -118,7 +121,8 @@ def test_random_configurations_match_the_oracle(seed):
     for i in range(N_CASES):
         cfg = _draw(rng)
         try:
-            st, info = _run_case(cfg, with_bias=i % 3 == 0)
+            st, info = _run_case(cfg, with_bias=i % 3 == 0, epi_groups=(i // 3) % 3,
+                                 k_serpentine=(i // 2) % 2)
         except sg.GemmError as e:
             if e.status in (sg.GEMM_ERR_INVALID_ARG, sg.GEMM_ERR_SMEM_BUDGET):
                 skipped += 1
