@@ -84,16 +84,23 @@ def _code_only(text: str) -> str:
     return "\n".join(line for line in lines if line)
 
 
+def _portable_flags() -> str:
+    """The compiler flags with the include directories named relative to the
+    repository, so that a checkout in another directory hashes the same."""
+    rel = {CSRC: "software_pipelined_tiled_gemm_gb300/csrc", INCLUDE: "include"}
+    return " ".join(ARCH + [rel.get(f, f) for f in FLAGS])
+
+
 def kernel_digest() -> str:
     """Hash of the GEMM kernel's device code only (what an ncu capture of the
-    kernel depends on): comments and layout do not count, and the host planner
-    is left out."""
+    kernel depends on): comments and layout do not count, the host planner is
+    left out, and so is the directory the repository sits in."""
     h = hashlib.sha256()
     for f in KERNEL_FILES:
         h.update(f.encode())
         with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(_portable_flags().encode())
     return h.hexdigest()[:16]
 
 

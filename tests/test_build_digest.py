@@ -34,3 +34,19 @@ def test_escaped_quote_does_not_end_a_literal():
 def test_digest_is_stable_and_short():
     d = _build.kernel_digest()
     assert d == _build.kernel_digest() and len(d) == 16
+
+
+def test_digest_does_not_depend_on_the_checkout_directory(tmp_path):
+    # The committed ncu figures are looked up by this digest on whatever
+    # machine runs the bench, where the repository sits in another directory.
+    import importlib.util
+    import shutil
+    pkg = tmp_path / "elsewhere" / "software_pipelined_tiled_gemm_gb300"
+    shutil.copytree(_build.CSRC, pkg / "csrc")
+    shutil.copy(_build.__file__, pkg / "_build.py")
+    shutil.copytree(_build.INCLUDE, tmp_path / "elsewhere" / "include")
+    spec = importlib.util.spec_from_file_location("moved_build", pkg / "_build.py")
+    moved = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(moved)
+    assert moved.CSRC != _build.CSRC
+    assert moved.kernel_digest() == _build.kernel_digest()
