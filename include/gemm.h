@@ -247,6 +247,39 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
 /* Describe the plan's launch configuration. */
 gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info);
 
+/* ---- Planning without a plan ------------------------------------------------
+ * None of the pages has a counterpart to these calls; they expose the
+ * planner that gemm_plan_create runs, for capacity planning and for testing
+ * it on a machine without a GPU.
+ *
+ * The properties of a device that the planner reads. */
+typedef struct {
+  int sm_count;       /* streaming multiprocessors (cudaDeviceProp::multiProcessorCount) */
+  int smem_optin;     /* opt-in dynamic shared memory per block, bytes
+                         (cudaDevAttrMaxSharedMemoryPerBlockOptin) */
+  int64_t l2_bytes;   /* L2 cache size, bytes (cudaDeviceProp::l2CacheSize) */
+  int pair_clusters;  /* 2-CTA clusters the CTA-pair kernels can keep resident at once
+                         (cudaOccupancyMaxActiveClusters; every kernel runs one CTA per SM) */
+} gemm_device_desc_t;
+
+/* Fill *desc from `device`.  GEMM_ERR_UNSUPPORTED unless it is an sm_103
+ * device; GEMM_ERR_CUDA if a query fails. */
+gemm_status_t gemm_device_query(int device, gemm_device_desc_t* desc);
+
+/* What gemm_plan_create_ex with these arguments would choose on a device
+ * with the properties in *desc, written to *info exactly as
+ * gemm_plan_get_info reports it for a plan that has not run yet (the fields
+ * about the last run -- pads_operands, tma_store, kernels_per_run,
+ * host_panels -- are 0).  Argument errors are the same as
+ * gemm_plan_create_ex's, plus GEMM_ERR_INVALID_ARG for a NULL desc or info
+ * or a description field out of range (sm_count, smem_optin < 1;
+ * l2_bytes, pair_clusters < 0).  Makes no CUDA call, allocates nothing and
+ * does not check the device's architecture. */
+gemm_status_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 gemm_epilogue_t epi, int stages, gemm_variant_t variant,
+                                 const gemm_tuning_t* tuning, const gemm_device_desc_t* desc,
+                                 gemm_plan_info_t* info);
+
 /* Free everything the plan owns.  NULL is allowed.  Waits for the plan's
  * device work to finish first. */
 void gemm_plan_destroy(gemm_plan_t* plan);

@@ -16,7 +16,9 @@ B (N,K), caches a plan per problem, and launches on the current stream --
 the operation of the TileLang tutorial's ``matmul_auto`` (A (M,K), B (N,K),
 ``T.gemm(..., transpose_B=True)``) with an optional tanh-GELU or ReLU
 epilogue and fp16/bf16 or fp32 output.  :func:`matmul_nn` takes B as (K,N),
-the form of the Mosaic GPU guide's matmul example.
+the form of the Mosaic GPU guide's matmul example.  :func:`describe` reports
+what a plan would choose, for this GPU or for a device described by its
+properties (no GPU needed).
 """
 from __future__ import annotations
 
@@ -31,6 +33,7 @@ __all__ = [
     "gemm_plan_check",
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
+    "gemm_device_query", "gemm_plan_describe", "GemmDeviceDesc", "describe",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
     "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
     "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH", "GEMM_EPI_RELU",
@@ -78,6 +81,14 @@ class GemmPlanInfo(ctypes.Structure):
                 ("k_sub", ctypes.c_int), ("host_panels", ctypes.c_int),
                 ("k_serpentine", ctypes.c_int), ("l2_prefetch_first", ctypes.c_int),
                 ("sk_cluster", ctypes.c_int), ("epi_groups", ctypes.c_int)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class GemmDeviceDesc(ctypes.Structure):
+    _fields_ = [("sm_count", ctypes.c_int), ("smem_optin", ctypes.c_int),
+                ("l2_bytes", ctypes.c_int64), ("pair_clusters", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -144,6 +155,12 @@ def load_library(path: Optional[str] = None):
         lib.gemm_version.restype = ctypes.c_char_p
         lib.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
         lib.gemm_run_noalloc.restype = ci
+        lib.gemm_device_query.argtypes = [ci, ctypes.POINTER(GemmDeviceDesc)]
+        lib.gemm_device_query.restype = ci
+        lib.gemm_plan_describe.argtypes = [i64, i64, i64, ci, ci, ci, ci, ctypes.POINTER(GemmTuning),
+                                           ctypes.POINTER(GemmDeviceDesc),
+                                           ctypes.POINTER(GemmPlanInfo)]
+        lib.gemm_plan_describe.restype = ci
         _lib = lib
         return lib
 
@@ -235,6 +252,20 @@ def gemm_plan_destroy(plan):
     load_library().gemm_plan_destroy(plan)
 
 
+def gemm_device_query(device: int):
+    desc = GemmDeviceDesc()
+    st = load_library().gemm_device_query(int(device), ctypes.byref(desc))
+    return st, desc
+
+
+def gemm_plan_describe(M, N, K, dtype, epi, stages, variant, tuning, desc):
+    info = GemmPlanInfo()
+    st = load_library().gemm_plan_describe(M, N, K, dtype, epi, stages, variant,
+                                           ctypes.byref(tuning) if tuning is not None else None,
+                                           ctypes.byref(desc), ctypes.byref(info))
+    return st, info
+
+
 # ------------------------------------------------------------ torch layer --
 
 _DT = {"f16": GEMM_F16, "bf16": GEMM_BF16}
@@ -320,6 +351,36 @@ class Plan:
             self.close()
         except Exception:  # noqa: BLE001 - interpreter shutdown
             pass
+
+
+def describe(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", device=0,
+             **tuning) -> dict:
+    """What ``Plan(M, N, K, dtype, epilogue, stages, variant, device, **tuning)``
+    would choose, as :meth:`Plan.info` reports it, without creating the plan.
+
+    ``device``: a CUDA device index (its properties are queried), or a dict
+    or :class:`GemmDeviceDesc` with ``sm_count``, ``smem_optin``,
+    ``l2_bytes`` and ``pair_clusters`` -- then no CUDA call is made."""
+    if isinstance(device, GemmDeviceDesc):
+        desc = device
+    elif isinstance(device, dict):
+        desc = GemmDeviceDesc(**{k: int(device[k]) for k, _ in GemmDeviceDesc._fields_})
+    else:
+        st, desc = gemm_device_query(int(device))
+        _check(st, "gemm_device_query")
+    names = [k for k, _ in GemmTuning._fields_]
+    unknown = set(tuning) - set(names)
+    if unknown:
+        raise TypeError("unknown tuning keyword(s): %s" % ", ".join(sorted(unknown)))
+    t = GemmTuning(**{k: int(v) for k, v in tuning.items()})
+    st, info = gemm_plan_describe(int(M), int(N), int(K),
+                                  _DT[dtype] if isinstance(dtype, str) else int(dtype),
+                                  _EPI[epilogue] if not isinstance(epilogue, int) else int(epilogue),
+                                  int(stages),
+                                  _VAR[variant] if isinstance(variant, str) else int(variant), t,
+                                  desc)
+    _check(st, "gemm_plan_describe")
+    return info.as_dict()
 
 
 _plans = {}

@@ -329,13 +329,18 @@ size_t gemm_smem_bytes(int bm, int bn, int bk, int elem_bytes, int stages) {
          static_cast<size_t>(elem_bytes);
 }
 
-gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
-                                  gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
-                                  gemm_variant_t variant, int device,
-                                  const gemm_tuning_t* tuning) {
-  g_last_error.clear();
-  if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
+namespace {
+
+// Tuning requests, validated (0 = choose).
+struct Wants {
+  int bn = 0, group = 0, ctas = 0, cg = 0, split = 0;
+  unsigned long long timeout = kDefaultTimeoutNs;
+};
+
+// Checks everything about a plan request that needs no device.
+gemm_status_t check_create_args(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                gemm_epilogue_t epi, int stages, gemm_variant_t variant,
+                                const gemm_tuning_t* tuning, Wants* w) {
   gemm_status_t st = check_common(M, N, K, dtype, epi, stages);
   if (st != GEMM_OK) return st;
   if (variant != GEMM_PIPELINED && variant != GEMM_SINGLE_BUFFER)
@@ -343,24 +348,21 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   if (variant == GEMM_SINGLE_BUFFER && stages != 1)
     return fail(GEMM_ERR_INVALID_ARG, "the single-buffer variant has exactly 1 stage (got %d)",
                 stages);
-  if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
-  int want_bn = 0, want_group = 0, want_ctas = 0, want_cg = 0, want_split = 0;
-  unsigned long long timeout = kDefaultTimeoutNs;
   if (tuning) {
-    want_bn = tuning->tile_n;
-    want_group = tuning->raster_group;
-    want_ctas = tuning->max_ctas;
-    want_cg = tuning->cta_group;
-    want_split = tuning->tail_split;
-    if (want_split < -1 || want_split > kMaxTailSplits)
-      return fail(GEMM_ERR_INVALID_ARG, "tail_split %d not in {-1, 0, 1, 2, 3, 4}", want_split);
-    if (want_bn != 0 && want_bn != 64 && want_bn != 128 && want_bn != 256)
-      return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", want_bn);
-    if (want_cg < 0 || want_cg > 2)
-      return fail(GEMM_ERR_INVALID_ARG, "cta_group %d not in {0, 1, 2}", want_cg);
-    if (want_cg == 2 && want_bn == 64)
+    w->bn = tuning->tile_n;
+    w->group = tuning->raster_group;
+    w->ctas = tuning->max_ctas;
+    w->cg = tuning->cta_group;
+    w->split = tuning->tail_split;
+    if (w->split < -1 || w->split > kMaxTailSplits)
+      return fail(GEMM_ERR_INVALID_ARG, "tail_split %d not in {-1, 0, 1, 2, 3, 4}", w->split);
+    if (w->bn != 0 && w->bn != 64 && w->bn != 128 && w->bn != 256)
+      return fail(GEMM_ERR_INVALID_ARG, "tile_n %d not in {0, 64, 128, 256}", w->bn);
+    if (w->cg < 0 || w->cg > 2)
+      return fail(GEMM_ERR_INVALID_ARG, "cta_group %d not in {0, 1, 2}", w->cg);
+    if (w->cg == 2 && w->bn == 64)
       return fail(GEMM_ERR_INVALID_ARG, "CTA pairs use tile_n 128 or 256");
-    if (want_group < 0 || want_ctas < 0)
+    if (w->group < 0 || w->ctas < 0)
       return fail(GEMM_ERR_INVALID_ARG, "negative raster_group / max_ctas");
     if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
     if (tuning->debug_fault < 0 || tuning->debug_fault > 1)
@@ -374,19 +376,40 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     if (tuning->k_serpentine < -1 || tuning->k_serpentine > 1)
       return fail(GEMM_ERR_INVALID_ARG, "k_serpentine %d not in {-1, 0, 1}",
                   tuning->k_serpentine);
-    if (tuning->b_kn == 1 && want_split >= 2)
+    if (tuning->b_kn == 1 && w->split >= 2)
       return fail(GEMM_ERR_INVALID_ARG, "narrow tail tiles are not available with b_kn = 1");
-    if (tuning->timeout_ns > 0) timeout = static_cast<unsigned long long>(tuning->timeout_ns);
+    if (tuning->timeout_ns > 0) w->timeout = static_cast<unsigned long long>(tuning->timeout_ns);
   }
+  return GEMM_OK;
+}
 
-  int ndev = 0;
-  cudaError_t e = cudaGetDeviceCount(&ndev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
-  if (device >= ndev) return fail(GEMM_ERR_INVALID_ARG, "device %d >= count %d", device, ndev);
-  DeviceGuard guard(device);
-  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+// Co-resident 2-CTA clusters of the pair kernel of tile width bn with `smem`
+// bytes of dynamic shared memory per CTA.
+using PairClustersFn = gemm_status_t (*)(void* ctx, int bn, size_t smem, int* clusters);
+
+// From the device: ctx points to the device's opt-in shared-memory limit.
+gemm_status_t cuda_pair_clusters(void* ctx, int bn, size_t smem, int* clusters) {
+  cudaError_t e = set_smem(bn, 2, *static_cast<const size_t*>(ctx));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+  e = bn == 128 ? gemm_max_clusters_pair128(smem, clusters)
+                : gemm_max_clusters_pair256(smem, clusters);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+  return GEMM_OK;
+}
+
+// From a description: ctx points to a gemm_device_desc_t.  Every kernel
+// instance runs one CTA per SM (its registers allow no second one), so the
+// count does not depend on the tile width or the shared memory.
+gemm_status_t desc_pair_clusters(void* ctx, int, size_t, int* clusters) {
+  *clusters = static_cast<const gemm_device_desc_t*>(ctx)->pair_clusters;
+  return GEMM_OK;
+}
+
+// Properties of the current device (which must be `device`) that the
+// planner uses, except pair_clusters.  GEMM_ERR_UNSUPPORTED unless sm_103.
+gemm_status_t device_props(int device, gemm_device_desc_t* desc) {
   cudaDeviceProp prop;
-  e = cudaGetDeviceProperties(&prop, device);
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
   if (prop.major != 10 || prop.minor != 3)
     return fail(GEMM_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
@@ -394,7 +417,24 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   int smem_optin = 0;
   e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem optin)");
+  desc->sm_count = prop.multiProcessorCount;
+  desc->smem_optin = smem_optin;
+  desc->l2_bytes = prop.l2CacheSize;
+  desc->pair_clusters = 0;
+  return GEMM_OK;
+}
 
+// The planner: chooses the tile, ring, epilogue, walkers and last-wave
+// treatment of a plan for a device described by `dev`, and fills the
+// corresponding fields of *p.  Host arithmetic only, except what
+// `pair_clusters` does; allocates nothing (on failure *p is left to the
+// caller to discard).
+gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
+                          PairClustersFn pair_clusters, void* ctx, int64_t M, int64_t N,
+                          int64_t K, gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                          gemm_variant_t variant, const gemm_tuning_t* tuning, const Wants& w) {
+  const int want_bn = w.bn, want_group = w.group, want_ctas = w.ctas, want_cg = w.cg,
+            want_split = w.split;
   // Tile shape.  Candidates in order of preference: CTA pairs (256-row
   // tiles; each CTA holds half of B, so a slot is 32 KiB at tile_n 256 and
   // deeper rings fit) when at least half a wave of pair tiles exists, then
@@ -433,22 +473,19 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
                                               : 1);
     int bufs = 2;
     size_t need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
-    if (need > static_cast<size_t>(smem_optin)) {
+    if (need > static_cast<size_t>(dev.smem_optin)) {
       bufs = 1;
       need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
     }
-    if (need > static_cast<size_t>(smem_optin)) continue;
+    if (need > static_cast<size_t>(dev.smem_optin)) continue;
     const int64_t tiles =
         cdiv(std::max<int64_t>(M, 1), kBM * cg) * cdiv(std::max<int64_t>(N, 1), bn);
     int clusters = 0;
     if (cg == 2) {
       // Auto mode takes pairs only for problems with at least half a wave of pair tiles.
       if (want_cg == 0 && M <= kBM) continue;
-      e = set_smem(bn, cg, static_cast<size_t>(smem_optin));
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
-      e = bn == 128 ? gemm_max_clusters_pair128(need, &clusters)
-                    : gemm_max_clusters_pair256(need, &clusters);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+      const gemm_status_t cq = pair_clusters(ctx, bn, need, &clusters);
+      if (cq != GEMM_OK) return cq;
       if (clusters < 1) continue;
       if (want_cg == 0 && 2 * tiles < clusters) continue;
     }
@@ -461,12 +498,12 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     // Whole tiles that keep at least 80 % of the SMs busy are wide enough:
     // 128 x 16384 x 2048 runs 20.5 us on 128 tiles 128 wide, 26.1 us on 256
     // tiles 64 wide.
-    if (want_bn != 0 || cg == 2 || 10 * tiles >= 8 * static_cast<int64_t>(prop.multiProcessorCount))
+    if (want_bn != 0 || cg == 2 || 10 * tiles >= 8 * static_cast<int64_t>(dev.sm_count))
       break;
     // Few tiles: a width whose tiles can be split in two along K (see below)
     // and then keep at least 80 % of the SMs busy is wide enough.
     if (cg == 1 && variant == GEMM_PIPELINED && want_split != -1 &&
-        2 * tiles <= prop.multiProcessorCount && 10 * 2 * tiles >= 8 * prop.multiProcessorCount &&
+        2 * tiles <= dev.sm_count && 10 * 2 * tiles >= 8 * dev.sm_count &&
         cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
         static_cast<int64_t>(ring_stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
             static_cast<int64_t>(epi_cta_partial_bytes(bn, groups)))
@@ -475,13 +512,10 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   if (chosen == 0) {
     return fail(GEMM_ERR_SMEM_BUDGET,
                 "stages=%d does not fit %d B of shared memory at tile width %d (ring %zu B)",
-                stages, smem_optin, want_bn ? want_bn : 64,
+                stages, dev.smem_optin, want_bn ? want_bn : 64,
                 gemm_smem_bytes(kBM, want_bn ? want_bn : 64, kBK, 2, stages));
   }
 
-  gemm_plan* p = new (std::nothrow) gemm_plan();
-  if (!p) return fail(GEMM_ERR_INVALID_ARG, "out of host memory");
-  p->device = device;
   p->M = M;
   p->N = N;
   p->K = K;
@@ -490,8 +524,8 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->stages = stages;
   p->ring_stages = ring_stages;
   p->variant = variant;
-  p->sm_count = prop.multiProcessorCount;
-  p->timeout_ns = timeout;
+  p->sm_count = dev.sm_count;
+  p->timeout_ns = w.timeout;
   p->num_acc = variant == GEMM_SINGLE_BUFFER ? 1 : 2;
   p->max_ctas = want_ctas;
   p->debug_fault = tuning ? tuning->debug_fault : 0;
@@ -506,7 +540,6 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   p->tiles_n = cdiv(N, chosen);
   p->num_tiles = p->tiles_m * p->tiles_n;
   if (p->num_tiles > kMaxDim) {
-    delete p;
     return fail(GEMM_ERR_INVALID_ARG, "too many output tiles");
   }
   p->raster_group = want_group > 0 ? want_group : (chosen_cg == 2 ? 8 : 16);
@@ -582,7 +615,6 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     const int max_s = std::min(kMaxTailSplits, p->bn / kStoreCols);
     if (want_split == 1 || (want_split == 0 && sk_ok)) {
       if (!sk_ok && want_split == 1 && rem > 0) {
-        delete p;
         return fail(GEMM_ERR_INVALID_ARG,
                     "stream-K needs at least one full wave of tiles and a ring of >= %d B",
                     static_cast<int>(epi_cta_partial_bytes(p->bn, p->epi_groups)));
@@ -598,7 +630,6 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
         p->dp_tiles = p->num_tiles - rem;
         p->tail_splits = static_cast<int>(S);
       } else if (want_split >= 2) {
-        delete p;
         return fail(GEMM_ERR_INVALID_ARG,
                     "tail_split %d does not divide tile width %d into >= %d-column tiles",
                     want_split, p->bn, kStoreCols);
@@ -624,7 +655,7 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
     const int64_t wave_cols =
         std::min<int64_t>(p->tiles_n, cdiv(walkers, std::max(1, p->raster_group))) * p->bn;
     const double wave_bytes = static_cast<double>(wave_rows + wave_cols) * static_cast<double>(K) * 2.0;
-    const bool auto_on = p->num_tiles > walkers && wave_bytes > 0.5 * prop.l2CacheSize;
+    const bool auto_on = p->num_tiles > walkers && wave_bytes > 0.5 * static_cast<double>(dev.l2_bytes);
     p->k_serpentine =
         (p->tiles_m > 1 && (want_serp == 1 || (want_serp == 0 && auto_on))) ? 1 : 0;
   }
@@ -635,48 +666,75 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
   // prefetches would only queue ahead of the ring's copies (16896 x 512 x
   // 640: 13.0 -> 13.9 us).
   p->l2_prefetch_first = static_cast<double>(M + N) * static_cast<double>(K) * 2.0 >
-                                 0.75 * static_cast<double>(prop.l2CacheSize)
+                                 0.75 * static_cast<double>(dev.l2_bytes)
                              ? 1
                              : 0;
   const int64_t tail = p->num_tiles - p->dp_tiles;
   p->num_units = p->sk_tiles > 0 ? p->dp_tiles : p->dp_tiles + tail * p->tail_splits;
-  if (p->num_units > kMaxDim) {
-    delete p;
-    return fail(GEMM_ERR_INVALID_ARG, "too many work units");
-  }
+  if (p->num_units > kMaxDim) return fail(GEMM_ERR_INVALID_ARG, "too many work units");
   p->grid = chosen_cg * static_cast<int>(
                            std::min<int64_t>(p->sk_tiles > 0 ? walkers : p->num_units, walkers));
+  return GEMM_OK;
+}
+
+}  // namespace
+
+gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64_t K,
+                                  gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
+                                  gemm_variant_t variant, int device,
+                                  const gemm_tuning_t* tuning) {
+  g_last_error.clear();
+  if (!out) return fail(GEMM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Wants w;
+  gemm_status_t st = check_create_args(M, N, K, dtype, epi, stages, variant, tuning, &w);
+  if (st != GEMM_OK) return st;
+  if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device >= ndev) return fail(GEMM_ERR_INVALID_ARG, "device %d >= count %d", device, ndev);
+  DeviceGuard guard(device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  gemm_device_desc_t desc;
+  st = device_props(device, &desc);
+  if (st != GEMM_OK) return st;
+
+  gemm_plan* p = new (std::nothrow) gemm_plan();
+  if (!p) return fail(GEMM_ERR_INVALID_ARG, "out of host memory");
+  p->device = device;
+  size_t optin = static_cast<size_t>(desc.smem_optin);
+  st = plan_layout(p, desc, cuda_pair_clusters, &optin, M, N, K, dtype, epi, stages, variant,
+                   tuning, w);
+  if (st != GEMM_OK) {
+    delete p;
+    return st;
+  }
 
   // The limit is per kernel function, shared by every plan on the device:
   // always raise it to the device maximum, never to this plan's own size, so
   // a later plan with a smaller ring cannot lower it under an earlier one.
-  e = set_smem(p->bn, p->cg, static_cast<size_t>(smem_optin));
+  e = set_smem(p->bn, p->cg, static_cast<size_t>(desc.smem_optin));
   if (e != cudaSuccess) {
     delete p;
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
   }
+  // Device memory: the stream-K workspace and flags, and the status word.
+  // On a failure gemm_plan_destroy frees whatever was already allocated.
   if (p->sk_tiles > 0) {
-    const size_t nflags = static_cast<size_t>(p->sk_tiles) * chosen_cg * 4 * p->epi_groups;
+    const size_t nflags = static_cast<size_t>(p->sk_tiles) * p->cg * 4 * p->epi_groups;
     if ((e = cudaMalloc(&p->sk_ws, nflags * epi_warp_partial_bytes(p->bn, p->epi_groups))) !=
             cudaSuccess ||
         (e = cudaMalloc(&p->sk_flags, nflags * sizeof(int))) != cudaSuccess ||
         (e = cudaMemset(p->sk_flags, 0, nflags * sizeof(int))) != cudaSuccess) {
-      if (p->sk_ws) cudaFree(p->sk_ws);
-      if (p->sk_flags) cudaFree(p->sk_flags);
-      delete p;
+      gemm_plan_destroy(p);
       return cuda_fail(e, "cudaMalloc(stream-K workspace)");
     }
   }
-  e = cudaMalloc(&p->d_status, 4 * sizeof(int));
-  if (e != cudaSuccess) {
-    delete p;
+  if ((e = cudaMalloc(&p->d_status, 4 * sizeof(int))) != cudaSuccess ||
+      (e = cudaMemset(p->d_status, 0, 4 * sizeof(int))) != cudaSuccess) {
+    gemm_plan_destroy(p);
     return cuda_fail(e, "cudaMalloc(status)");
-  }
-  e = cudaMemset(p->d_status, 0, 4 * sizeof(int));
-  if (e != cudaSuccess) {
-    cudaFree(p->d_status);
-    delete p;
-    return cuda_fail(e, "cudaMemset(status)");
   }
   if (tuning) {
     p->tuning = *tuning;
@@ -1118,8 +1176,9 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
   return GEMM_OK;
 }
 
-gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info) {
-  if (!plan || !info) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+namespace {
+
+void fill_info(const gemm_plan* plan, gemm_plan_info_t* info) {
   info->tile_m = kBM * plan->cg;
   info->tile_n = plan->bn;
   info->tile_k = kBK;
@@ -1147,6 +1206,61 @@ gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info
   info->k_sub = plan->k_sub;
   info->host_panels = plan->num_panels >= 2 ? plan->num_panels : 0;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
+}
+
+}  // namespace
+
+gemm_status_t gemm_plan_get_info(const gemm_plan_t* plan, gemm_plan_info_t* info) {
+  if (!plan || !info) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+  fill_info(plan, info);
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_device_query(int device, gemm_device_desc_t* desc) {
+  g_last_error.clear();
+  if (!desc) return fail(GEMM_ERR_INVALID_ARG, "desc is NULL");
+  if (device < 0) return fail(GEMM_ERR_INVALID_ARG, "device %d < 0", device);
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device >= ndev) return fail(GEMM_ERR_INVALID_ARG, "device %d >= count %d", device, ndev);
+  DeviceGuard guard(device);
+  if (guard.err != cudaSuccess) return cuda_fail(guard.err, "cudaSetDevice");
+  gemm_device_desc_t d;
+  gemm_status_t st = device_props(device, &d);
+  if (st != GEMM_OK) return st;
+  // Any pair instance at one CTA per SM gives the count: the 256-wide tile's
+  // six-slice ring with four epilogue warps.
+  size_t optin = static_cast<size_t>(d.smem_optin);
+  const size_t smem = kernel_smem_bytes(256, 6, 2, 2, 1);
+  if (smem > optin) return fail(GEMM_ERR_UNSUPPORTED, "no pair instance fits %zu B", optin);
+  st = cuda_pair_clusters(&optin, 256, smem, &d.pair_clusters);
+  if (st != GEMM_OK) return st;
+  *desc = d;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 gemm_epilogue_t epi, int stages, gemm_variant_t variant,
+                                 const gemm_tuning_t* tuning, const gemm_device_desc_t* desc,
+                                 gemm_plan_info_t* info) {
+  g_last_error.clear();
+  if (!desc || !info) return fail(GEMM_ERR_INVALID_ARG, "NULL argument");
+  if (desc->sm_count < 1 || desc->smem_optin < 1 || desc->l2_bytes < 0 ||
+      desc->pair_clusters < 0)
+    return fail(GEMM_ERR_INVALID_ARG,
+                "device description out of range (sm_count %d, smem_optin %d, l2_bytes %lld, "
+                "pair_clusters %d)",
+                desc->sm_count, desc->smem_optin, static_cast<long long>(desc->l2_bytes),
+                desc->pair_clusters);
+  Wants w;
+  gemm_status_t st = check_create_args(M, N, K, dtype, epi, stages, variant, tuning, &w);
+  if (st != GEMM_OK) return st;
+  gemm_plan p;  // host fields only: nothing is allocated for it
+  st = plan_layout(&p, *desc, desc_pair_clusters, const_cast<gemm_device_desc_t*>(desc), M, N, K,
+                   dtype, epi, stages, variant, tuning, w);
+  if (st != GEMM_OK) return st;
+  fill_info(&p, info);
   return GEMM_OK;
 }
 

@@ -9,7 +9,7 @@
  *   abi_client layout
  *       Host-only checks: version, status strings, the shared-memory
  *       formula, argument rejection, and the size and field offsets of
- *       gemm_tuning_t and gemm_plan_info_t, printed one per line as
+ *       gemm_tuning_t, gemm_plan_info_t and gemm_device_desc_t, printed one per line as
  *       "key value" for the Python test to compare with its ctypes mirrors.
  *
  *   abi_client run M N K dtype epi a.bin b.bin c.bin
@@ -85,6 +85,12 @@ static int layout(void) {
   OFF(gemm_plan_info_t, "info", l2_prefetch_first);
   OFF(gemm_plan_info_t, "info", sk_cluster);
   OFF(gemm_plan_info_t, "info", epi_groups);
+
+  printf("sizeof device %lu\n", (unsigned long)sizeof(gemm_device_desc_t));
+  OFF(gemm_device_desc_t, "device", sm_count);
+  OFF(gemm_device_desc_t, "device", smem_optin);
+  OFF(gemm_device_desc_t, "device", l2_bytes);
+  OFF(gemm_device_desc_t, "device", pair_clusters);
   return 0;
 }
 

@@ -64,7 +64,8 @@ def test_c_program_sees_the_documented_host_behaviour(client):
     assert got["wait_mma_full"] == sg.gemm_wait_detail_string((2 << 16) | 2)
 
 
-@pytest.mark.parametrize("tag,mirror", [("tuning", sg.GemmTuning), ("info", sg.GemmPlanInfo)])
+@pytest.mark.parametrize("tag,mirror", [("tuning", sg.GemmTuning), ("info", sg.GemmPlanInfo),
+                                        ("device", sg.GemmDeviceDesc)])
 def test_struct_layout_matches_the_ctypes_mirror(client, tag, mirror):
     got = _layout(client)
     assert got[("sizeof", tag)] == ctypes.sizeof(mirror)
