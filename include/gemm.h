@@ -186,7 +186,16 @@ gemm_status_t gemm_plan_create_ex(gemm_plan_t** out, int64_t M, int64_t N, int64
  * A or B.  M, N, K, dtype, epi and stages must equal the plan's
  * (GEMM_ERR_PLAN_MISMATCH otherwise).  M == 0 or N == 0 is a no-op; K == 0
  * writes zeros (GELU(0) = 0).  Asynchronous: does not synchronise the
- * stream or the device. */
+ * stream or the device.
+ *
+ * CUDA graphs: gemm_run and gemm_run_bias may be captured into a graph
+ * (stream capture, any mode) and the graph replayed; each replay computes
+ * the GEMM of the buffers' contents at that time.  A plan whose operands
+ * need padded copies allocates that scratch in its first run (and again
+ * when a later run needs more), so run such a plan once before capturing
+ * it.  Consecutive GEMMs on one stream may be launched early (programmatic
+ * dependent launch), but each waits for its predecessor's results before
+ * reading memory, so one GEMM's C may be the next one's A or B. */
 gemm_status_t gemm_run(gemm_plan_t* plan, const void* A, const void* B, void* C,
                        int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                        gemm_epilogue_t epi, int stages, void* stream);
