@@ -22,6 +22,7 @@ properties (no GPU needed).
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 import threading
@@ -34,6 +35,7 @@ __all__ = [
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
     "gemm_device_query", "gemm_plan_describe", "GemmDeviceDesc", "describe",
+    "get_plan", "set_plan_cache_limit", "clear_plan_cache", "plan_cache_size",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
     "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
     "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH", "GEMM_EPI_RELU",
@@ -383,8 +385,44 @@ def describe(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", devic
     return info.as_dict()
 
 
-_plans = {}
+# Plans cached by get_plan (and so by matmul_nt / matmul_nn), least recently
+# used first.  Each plan holds device memory (its status word; a stream-K
+# workspace of up to a few tens of MiB; staging for run_host), so a caller
+# with many distinct shapes can bound the cache.  Unbounded by default: a
+# plan captured in a CUDA graph must outlive the graph, and closing a plan
+# synchronises its device, which is not allowed during stream capture.
+_plans: "collections.OrderedDict" = collections.OrderedDict()
 _plans_lock = threading.Lock()
+_plans_limit = 0
+
+
+def set_plan_cache_limit(n: int) -> None:
+    """Keep at most n cached plans (0: no limit), closing the least recently
+    used ones beyond it, now and on later insertions.  Do not use a limit
+    while graphs that captured cached plans are alive."""
+    global _plans_limit
+    if int(n) < 0:
+        raise ValueError("the plan cache limit must be >= 0")
+    with _plans_lock:
+        _plans_limit = int(n)
+        _evict_locked()
+
+
+def clear_plan_cache() -> None:
+    """Close every cached plan (synchronises their devices)."""
+    with _plans_lock:
+        while _plans:
+            _plans.popitem(last=False)[1].close()
+
+
+def plan_cache_size() -> int:
+    with _plans_lock:
+        return len(_plans)
+
+
+def _evict_locked() -> None:
+    while _plans_limit and len(_plans) > _plans_limit:
+        _plans.popitem(last=False)[1].close()
 
 
 def matmul_nn(A, B, epilogue=None, stages: int = 6, out=None, out_dtype=None, bias=None,
@@ -407,6 +445,9 @@ def get_plan(M, N, K, dtype, epilogue=None, stages=4, variant="pipelined", devic
         if p is None:
             p = Plan(M, N, K, dtype, epilogue, stages, variant, device, **tuning)
             _plans[key] = p
+            _evict_locked()
+        else:
+            _plans.move_to_end(key)
         return p
 
 

@@ -153,3 +153,36 @@ def test_matmul_nt_checks_arguments_on_cpu_tensors():
     b = torch.zeros(4, 8, dtype=torch.float16)
     with pytest.raises(ValueError):
         sg.matmul_nt(a, b)
+
+
+def test_plan_cache_is_lru_and_bounded_on_request(monkeypatch):
+    # get_plan's cache logic with a stand-in for Plan (creating a real plan needs a GPU)
+    closed = []
+
+    class FakePlan:
+        def __init__(self, M, *args, **kw):
+            self.M = M
+
+        def close(self):
+            closed.append(self.M)
+
+    monkeypatch.setattr(sg, "Plan", FakePlan)
+    sg.clear_plan_cache()
+    try:
+        p1 = sg.get_plan(1, 8, 8, "f16")
+        assert sg.get_plan(1, 8, 8, "f16") is p1           # cached
+        for m in (2, 3, 4):
+            sg.get_plan(m, 8, 8, "f16")
+        assert sg.plan_cache_size() == 4 and closed == []  # unbounded by default
+        sg.get_plan(1, 8, 8, "f16")                        # 1 becomes the most recent
+        sg.set_plan_cache_limit(2)                         # evicts the two least recent: 2, 3
+        assert closed == [2, 3] and sg.plan_cache_size() == 2
+        sg.get_plan(5, 8, 8, "f16")                        # evicts 4
+        assert closed == [2, 3, 4]
+        assert sg.get_plan(1, 8, 8, "f16") is p1
+        with pytest.raises(ValueError):
+            sg.set_plan_cache_limit(-1)
+    finally:
+        sg.set_plan_cache_limit(0)
+        sg.clear_plan_cache()
+    assert sorted(closed) == [1, 2, 3, 4, 5] and sg.plan_cache_size() == 0
