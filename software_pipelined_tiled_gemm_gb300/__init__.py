@@ -34,7 +34,7 @@ __all__ = [
     "gemm_plan_check",
     "gemm_plan_get_info", "gemm_plan_destroy", "gemm_status_string", "gemm_smem_bytes",
     "gemm_last_error", "gemm_version", "gemm_run_noalloc", "GemmTuning", "GemmPlanInfo",
-    "gemm_device_query", "gemm_plan_describe", "GemmDeviceDesc", "describe",
+    "gemm_device_query", "gemm_plan_describe", "GemmDeviceDesc", "describe", "GB300",
     "get_plan", "set_plan_cache_limit", "clear_plan_cache", "plan_cache_size",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
     "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
@@ -86,6 +86,13 @@ class GemmPlanInfo(ctypes.Structure):
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+# What gemm_device_query reports on a GB300 (sm_103): 152 SMs, 227 KiB of
+# opt-in shared memory per block, the L2 size the driver reports, 76
+# co-resident 2-CTA clusters.  describe() and the planning CLI use it to plan
+# for a GB300 on a machine without one.
+GB300 = dict(sm_count=152, smem_optin=232448, l2_bytes=135528448, pair_clusters=76)
 
 
 class GemmDeviceDesc(ctypes.Structure):

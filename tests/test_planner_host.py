@@ -20,8 +20,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # cudaDeviceProp / occupancy figures of a GB300 (sm_103): 152 SMs, 227 KiB of
 # opt-in shared memory per block, the L2 size the driver reports, and one
-# 2-CTA cluster per SM pair.
-GB300 = dict(sm_count=152, smem_optin=232448, l2_bytes=135528448, pair_clusters=76)
+# 2-CTA cluster per SM pair (the package's description; a GPU test checks it).
+GB300 = dict(sg.GB300)
 
 
 def describe(M, N, K, dtype="f16", device=None, **kw):
