@@ -50,7 +50,12 @@ def test_gpu_bench_line_has_the_contract_keys():
     r = d["roofline"]
     assert r["bound"] in ("tensor", "hbm") and r["unit"] in ("TFLOP/s", "GB/s")
     assert 0 < r["frac"] < 1.5 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-6
-    assert r["traffic"] is None or r["traffic"] > 0
+    # the DRAM bytes of the committed ncu summary, whenever it was taken on the
+    # current kernel code (the digest must not depend on where the repository sits)
+    sys.path.insert(0, ROOT)
+    import bench
+    from software_pipelined_tiled_gemm_gb300 import _build
+    assert r["traffic"] == bench.traffic_from_profiles("gemm_4096_f16", _build.kernel_digest())
     # one GEMM launch per step (the operands are aligned: no padding copy)
     assert d["gpu_launches"] == steps
     # the oracle timed on the host cores
@@ -74,3 +79,28 @@ def test_reference_arm_times_the_oracle_on_cpu():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_lookup_follows_the_kernel_digest(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    from software_pipelined_tiled_gemm_gb300 import _build
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k.md").write_text(
+        "# summary\n"
+        "bench-traffic: kernel=k<1> workload=w source_digest=abc dram_bytes_per_launch=123\n"
+        "bench-traffic: kernel=k<1> workload=w:nn source_digest=abc dram_bytes_per_launch=456\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profiles("w", "abc") == 123
+    assert bench.traffic_from_profiles("w:nn", "abc") == 456
+    assert bench.traffic_from_profiles("w", "other") is None      # kernel changed since
+    assert bench.traffic_from_profiles("x", "abc") is None        # no summary
+    monkeypatch.undo()
+    # the committed summaries: each line's figure is found for its own workload
+    digest = _build.kernel_digest()
+    for fn in os.listdir(os.path.join(ROOT, "profiles")):
+        for line in open(os.path.join(ROOT, "profiles", fn)):
+            if line.startswith("bench-traffic:"):
+                kv = dict(x.split("=", 1) for x in line.split()[1:])
+                want = int(kv["dram_bytes_per_launch"]) if kv["source_digest"] == digest else None
+                assert bench.traffic_from_profiles(kv["workload"], digest) == want
