@@ -41,6 +41,13 @@ MUTANTS = {
                             "apply_epilogue(s, epilogue) + bias_of(bias, j, dtype)"),
     "bias_ignored": ("return bias ? oracle_decode(bias[j], dtype) : 0.0;", "return 0.0;"),
     "bias_entries_by_row": ("s + bias_of(bias, cols[t], dtype)", "s + bias_of(bias, rows[t], dtype)"),
+    "accumulate_in_float": ("      double s = 0.0;\n      for (int64_t k = 0; k < K; ++k) s += a[k] * b[k];\n      C[i * N + j]",
+                            "      float s = 0.0f;\n      for (int64_t k = 0; k < K; ++k) s += (float)(a[k] * b[k]);\n      C[i * N + j]"),
+    "overflow_saturates": ("if (v > max_finite) return (uint16_t)(sign | inf_bits);",
+                           "if (v > max_finite) return (uint16_t)(sign | (inf_bits - 1u));"),
+    "f16_subnormal_scale": ("v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
+    "nan_rounds_to_inf": ("if (isnan(x)) return (uint16_t)(inf_bits | (1u << (mant_bits - 1)));",
+                          "if (isnan(x)) return inf_bits;"),
 }
 
 PIN_TESTS = [
@@ -48,6 +55,7 @@ PIN_TESTS = [
     lambda: pins.test_bf16_decode_all_patterns_match_binary32_top_half(),
     lambda: pins.test_f16_round_matches_numpy_rne(),
     lambda: pins.test_bf16_round_is_nearest_even_by_enumeration(),
+    lambda: pins.test_rounding_of_nan_and_infinities(),
     lambda: pins.test_rounding_reproduces_printed_gelu_constants(),
     lambda: pins.test_gemm_matches_exact_rational_arithmetic("f16", (7, 5, 3)),
     lambda: pins.test_gemm_bit_exact_on_a_dyadic_grid("bf16"),

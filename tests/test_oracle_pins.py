@@ -71,6 +71,20 @@ def test_f16_round_matches_numpy_rne():
     assert np.array_equal(ours, ref)
 
 
+def test_rounding_of_nan_and_infinities():
+    # IEEE 754: a NaN stays a NaN (the default quiet NaN), infinities keep
+    # their sign.  fp16 against numpy's binary16 conversion; bf16 against the
+    # upper half of numpy's binary32 patterns (bf16 is binary32's top 16 bits,
+    # and these values need no rounding).
+    x = np.array([np.nan, np.inf, -np.inf], dtype=np.float64)
+    assert np.array_equal(oracle.round_to(x, "f16"), x.astype(np.float16).view(np.uint16))
+    top = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(oracle.round_to(x, "bf16"), top)
+    for dt in ("f16", "bf16"):
+        back = oracle.decode(oracle.round_to(x, dt), dt)
+        assert np.isnan(back[0]) and back[1] == np.inf and back[2] == -np.inf
+
+
 def test_bf16_round_is_nearest_even_by_enumeration():
     # All finite non-negative bf16 values, in increasing order of bit pattern.
     pos_bits = np.arange(0, 0x7f80, dtype=np.uint32)
