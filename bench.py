@@ -123,16 +123,38 @@ def traffic_from_profiles(workload, digest):
     return None
 
 
+# nvmlClocksEventReason* bits that matter for a measurement
+NVML_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
+
+
+def nvml_reason_names(bits):
+    return [n for b, n in sorted(NVML_REASON_BITS.items()) if bits & b]
+
+
+def summarize_clocks(samples, t0, t1, max_mhz):
+    """Clock record of a timed region from (time, sm_mhz, power_w, [reasons])
+    samples: the samples inside [t0, t1], or -- when the region is shorter
+    than the sampling period -- the two nearest to its middle."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": max_mhz, "reasons": ["no samples"]}
+    inside = [x for x in samples if t0 is not None and t0 <= x[0] <= t1]
+    window = "timed region"
+    if not inside:
+        mid = (t0 + t1) / 2 if t0 is not None else samples[-1][0]
+        inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
+        window = "nearest to the timed region"
+    return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max_mhz,
+            "reasons": sorted({n for x in inside for n in x[3]}), "samples": len(inside),
+            "window": window, "power_w_max": max(x[2] for x in inside)}
+
+
 class NvmlClockSampler:
     """SM clock, power and clock-event reasons read from NVML (the driver's
     libnvidia-ml, through ctypes; read-only queries) by a thread every 2 ms,
     kept only when they fall inside the timed region.  A region of a few tens
     of milliseconds -- a short bench run -- is too short for nvidia-smi's
     polling, which then yields one or two samples from outside the load."""
-
-    # nvmlClocksEventReason* bits
-    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown",
-                   0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
 
     def __init__(self, pci_bus_id, index):
         import ctypes
@@ -167,7 +189,8 @@ class NvmlClockSampler:
             self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
             self.reasons_fn(self.h, ct.byref(rs))
             if ok:
-                self.samples.append((time.time(), float(clk.value), mw.value / 1000.0, int(rs.value)))
+                self.samples.append((time.time(), float(clk.value), mw.value / 1000.0,
+                                     nvml_reason_names(int(rs.value))))
             time.sleep(0.002)
 
     def start(self):
@@ -187,18 +210,9 @@ class NvmlClockSampler:
             self.lib.nvmlShutdown()
         except Exception:
             pass
-        inside = [x for x in self.samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
-        window = "timed region"
-        if not inside:
-            if not self.samples:
-                return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"]}
-            mid = (self.t0 + self.t1) / 2 if self.t0 is not None else self.samples[-1][0]
-            inside = sorted(self.samples, key=lambda x: abs(x[0] - mid))[:2]
-            window = "nearest to the timed region"
-        reasons = sorted({n for x in inside for b, n in self.REASON_BITS.items() if x[3] & b})
-        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(inside), "window": window,
-                "power_w_max": max(x[2] for x in inside), "source": "nvml"}
+        out = summarize_clocks(self.samples, self.t0, self.t1, self.max_mhz)
+        out["source"] = "nvml"
+        return out
 
 
 def make_clock_sampler(dev, index):
@@ -247,6 +261,20 @@ class ClockSampler:
     def mark_stop(self):
         self.t1 = time.time()
 
+    @classmethod
+    def parse_rows(cls, text):
+        """(time, sm_mhz, max_mhz, power_w, [reasons]) from nvidia-smi's CSV
+        rows (the FIELDS columns, no header, no units); bad rows skipped."""
+        samples = []
+        for r in (line.split(",") for line in text.splitlines() if line.strip()):
+            try:
+                samples.append((cls._parse_ts(r[0]), float(r[2]), float(r[3]), float(r[4]),
+                                [n for i, n in enumerate(cls.REASONS)
+                                 if len(r) > 6 + i and r[6 + i].strip().lower() == "active"]))
+            except (ValueError, IndexError):
+                continue
+        return samples
+
     @staticmethod
     def _parse_ts(text):
         # "YYYY/MM/DD HH:MM:SS.mmm", local time of this host
@@ -266,30 +294,11 @@ class ClockSampler:
             self.proc.kill()
         self.tmp.flush()
         self.tmp.seek(0)
-        rows = [r.split(",") for r in self.tmp.read().splitlines() if r.strip()]
+        samples = self.parse_rows(self.tmp.read())
         os.unlink(self.tmp.name)
-        samples = []
-        for r in rows:
-            try:
-                ts = self._parse_ts(r[0])
-                samples.append((ts, float(r[2]), float(r[3]), float(r[4]),
-                                [n for i, n in enumerate(self.REASONS)
-                                 if len(r) > 6 + i and r[6 + i].strip().lower() == "active"]))
-            except (ValueError, IndexError):
-                continue
-        if not samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        inside = [x for x in samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
-        window = "timed region"
-        if not inside:  # region shorter than the sampling period: nearest samples
-            mid = (self.t0 + self.t1) / 2 if self.t0 is not None else samples[-1][0]
-            inside = sorted(samples, key=lambda x: abs(x[0] - mid))[:2]
-            window = "nearest to the timed region"
-        reasons = sorted({n for x in inside for n in x[4]})
-        return {"sm_mhz": statistics.median(x[1] for x in inside),
-                "sm_max_mhz": max(x[2] for x in samples),
-                "reasons": reasons, "samples": len(inside), "window": window,
-                "power_w_max": max(x[3] for x in inside)}
+        max_mhz = max((x[2] for x in samples), default=None)
+        return summarize_clocks([(t, mhz, w, rs) for t, mhz, _, w, rs in samples],
+                                self.t0, self.t1, max_mhz)
 
 
 def reduce_max(value, world_size, device=None):
