@@ -37,6 +37,9 @@ METRIC = "GEMM TFLOP/s (2MNK/time) at fp16 8192^3 on 1 GB300; % of dense tensor-
 UNIT = "TFLOP/s"
 FALLBACK_TFLOPS = 1900.0
 FALLBACK_HBM = 6800.0
+NOMINAL_TFLOPS = 2250.0            # dense fp16/bf16, no sparsity
+NOMINAL_HBM_GBS = 7900.0
+TENSOR_FLOP_PER_SM_CYCLE = 8192    # dense fp16/bf16 tcgen05 rate of one SM
 L2_BYTES = 126 * 1024 * 1024
 
 
@@ -72,6 +75,8 @@ def parse():
     ap.add_argument("--no-cublas", action="store_true",
                     help="skip the torch.matmul (cuBLAS) context timing")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--sustained-seconds", type=float, default=1.5,
+                    help="length of the back-to-back sustained window (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -318,37 +323,63 @@ def job_throughput(flops_per_step, steps, world_size, elapsed_ms):
     return flops_per_step * steps * world_size / (elapsed_ms * 1e-3) / 1e12
 
 
-def cpu_baseline(A, B, w, seconds, threads=0, epi=None):
+def cpu_baseline(A, B, w, seconds, threads=0, epi=None, bias=None):
     """Time the oracle (as it is) on a block of output rows of this workload
-    (A is (M, K), B is (N, K))."""
+    (A is (M, K), B is (N, K)): the first and the last `rows` / 2 rows, so the
+    sample reaches both the first tiles and the last wave's.  Returns the
+    record, the row indices and the oracle's fp64 values of those rows."""
     import oracle
+    import torch
     oracle.build()
     # calibrate on a few rows, then size the sample to about `seconds`
     probe = max(1, min(w.M, max(2, oracle.max_threads())))
     t0 = time.perf_counter()
-    oracle.gemm_nt(A[:probe], B, w.dtype, epilogue=epi, threads=threads)
+    oracle.gemm_nt(A[:probe], B, w.dtype, epilogue=epi, threads=threads, bias=bias)
     dt = max(time.perf_counter() - t0, 1e-3)
     rows = int(max(1, min(w.M, probe * seconds / dt)))
+    head = (rows + 1) // 2
+    idx = sorted(set(range(head)) | set(range(w.M - (rows - head), w.M)))
+    block = torch.cat([A[:head], A[w.M - (rows - head):]]) if rows > head else A[:head]
     t0 = time.perf_counter()
-    oracle.gemm_nt(A[:rows], B, w.dtype, epilogue=epi, threads=threads)
+    ref = oracle.gemm_nt(block, B, w.dtype, epilogue=epi, threads=threads, bias=bias)
     el = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
     cores = oracle.max_threads()
     out = {"value": flops / el / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-           "sample": "%d of %d output rows (all %d columns, full K=%d), %.1f s" % (
-               rows, w.M, w.N, w.K, el)}
+           "sample": "%d of %d output rows (the first %d and the last %d; all %d columns, "
+                     "full K=%d), %.1f s" % (rows, w.M, head, rows - head, w.N, w.K, el)}
     # The same oracle on one core, on a smaller block (about seconds / 5).
     t0 = time.perf_counter()
-    oracle.gemm_nt(A[:1], B, w.dtype, epilogue=epi, threads=1)
+    oracle.gemm_nt(A[:1], B, w.dtype, epilogue=epi, threads=1, bias=bias)
     dt1 = max(time.perf_counter() - t0, 1e-3)
     rows1 = int(max(1, min(w.M, seconds / 5 / dt1)))
     t0 = time.perf_counter()
-    oracle.gemm_nt(A[:rows1], B, w.dtype, epilogue=epi, threads=1)
+    oracle.gemm_nt(A[:rows1], B, w.dtype, epilogue=epi, threads=1, bias=bias)
     el1 = time.perf_counter() - t0
     oracle.gemm_nt(A[:1], B, w.dtype, epilogue=epi, threads=cores)  # restore the thread count
     out["single_thread"] = {"value": 2.0 * rows1 * w.N * w.K / el1 / 1e12, "unit": UNIT,
                             "sample": "%d output rows, %.1f s" % (rows1, el1)}
-    return out, rows
+    return out, idx, ref
+
+
+def parity_of_rows(C_rows, ref, dtype, f32):
+    """Per-element and Frobenius error of the rows of a result against the
+    oracle's values of the same rows (the tolerance the parity tests use)."""
+    import numpy as np
+    import oracle
+    from tests import tolerance
+    if f32:
+        got = C_rows.numpy().astype(np.float64)
+        kind = "f32"
+    else:
+        import torch
+        got = oracle.decode(C_rows.contiguous().view(torch.int16).numpy().view(np.uint16), dtype)
+        kind = dtype
+    st = tolerance.compare(got, ref, kind)
+    return {"ok": st["ok"], "elements": int(got.size), "max_ulp": st["max_ulp"],
+            "max_abs": st["max_abs"], "frob": st["frob"], "bad": st["bad"],
+            "tolerance": "|gpu - oracle| <= 2 ulp(|oracle|) + 1e-3 per element; relative "
+                         "Frobenius <= 1e-3"}
 
 
 def run_reference(args, w, ws, rank):
@@ -432,7 +463,8 @@ def main():
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
     a_p, b_p, c_p = A.data_ptr(), B.data_ptr(), C.data_ptr()
-    bias_t = gemm_inputs.bias(w.N, w.dtype, seed=w.seed).to(dev) if args.bias else None
+    bias_cpu = gemm_inputs.bias(w.N, w.dtype, seed=w.seed) if args.bias else None
+    bias_t = bias_cpu.to(dev) if bias_cpu is not None else None
     bias_p = bias_t.data_ptr() if bias_t is not None else 0
     operand_bytes = (w.M * w.K + w.N * w.K) * 2
     flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and operand_bytes <= L2_BYTES)
@@ -485,6 +517,8 @@ def main():
     if ds != 0:
         raise SystemExit("device status %d (detail %#x) after timed steps" % (ds, detail))
     elapsed_ms = reduce_max(elapsed_ms, ws, dev)
+    # The result of the last timed step, for the parity check below.
+    C_timed = C.cpu()
 
     flops = 2.0 * w.M * w.N * w.K
     value = job_throughput(flops, args.steps, ws, elapsed_ms)
@@ -568,8 +602,51 @@ def main():
                "d2h_bytes_per_step": w.M * w.N * C.element_size()}
 
     peaks, peak_src = load_peaks()
-    sustained = elapsed_ms > 1000.0
-    peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+
+    # Sustained: the same plan back to back for about --sustained-seconds,
+    # long enough for the power controller to settle at its cap, with a
+    # clock record of its own; reported against the measured sustained
+    # cuBLAS rate.  The burst region above is too short for the power
+    # sensor, so its clock record shows the boost clock.
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(10, int(args.sustained_seconds * 1e3 / max(kavg, 1e-3)))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        sclk = make_clock_sampler(dev, local)
+        sclk.start()
+        barrier()
+        torch.cuda.synchronize(dev)
+        sclk.mark_start()
+        s0.record(stream)
+        for _ in range(n_sus):
+            plan.run_ptr(a_p, b_p, c_p, sptr, bias_p)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        sclk.mark_stop()
+        barrier()
+        sus_clk = sclk.stop()
+        ds, detail = plan.check()
+        if ds != 0:
+            raise SystemExit("device status %d (detail %#x) after sustained steps" % (ds, detail))
+        sus_ms = reduce_max(s0.elapsed_time(s1), ws, dev)
+        sus_val = job_throughput(flops, n_sus, ws, sus_ms)
+        sus_peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+        sustained = {"value": sus_val, "unit": UNIT, "steps": n_sus, "seconds": sus_ms * 1e-3,
+                     "peak": sus_peak, "frac": sus_val / ws / sus_peak,
+                     "peak_source": "%s bf16_tflops_sustained" % peak_src,
+                     "l2": "back to back, no flush", "clocks": sus_clk}
+        mhz = sus_clk.get("sm_mhz")
+        if mhz:
+            # Rate per clock: TFLOP/s per GHz of the median SM clock, and the
+            # fraction of the tensor pipes' rate at that clock (152 SMs x 8192
+            # flop per SM-cycle for dense fp16/bf16).
+            sustained["tflops_per_ghz"] = sus_val / ws / (mhz * 1e-3)
+            sustained["frac_of_pipe_at_clock"] = (
+                sus_val / ws / (info["sm_count"] * TENSOR_FLOP_PER_SM_CYCLE * mhz * 1e6 / 1e12))
+
+    long_region = elapsed_ms > 1000.0
+    peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
     peak = float(peaks.get(peak_key, FALLBACK_TFLOPS))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM))
     digest = source_digest()
@@ -596,11 +673,37 @@ def main():
                     peak_src, peak_key),
                 "kernel_ms_avg": kavg, "kernels_per_step": info["kernels_per_run"]}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    # Beside the measured denominators: the published nominal rate, and the
+    # tensor pipes' rate at the maximum SM clock.
+    max_mhz = float(clk.get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0)
+    if roof["bound"] == "tensor":
+        roof["nominal_peak"] = NOMINAL_TFLOPS
+        roof["frac_of_nominal"] = achieved / NOMINAL_TFLOPS
+        roof["nominal_source"] = ("GB300 dense fp16/bf16 tensor rate without sparsity, "
+                                  "%.0f TFLOP/s (NVIDIA's published figure)" % NOMINAL_TFLOPS)
+        clock_peak = info["sm_count"] * TENSOR_FLOP_PER_SM_CYCLE * max_mhz * 1e6 / 1e12
+        roof["clock_peak"] = clock_peak
+        roof["frac_of_clock_peak"] = achieved / clock_peak
+        roof["clock_peak_source"] = ("%d SMs x %d flop per SM-cycle x %.0f MHz (maximum SM clock)"
+                                     % (info["sm_count"], TENSOR_FLOP_PER_SM_CYCLE, max_mhz))
+    else:
+        roof["nominal_peak"] = NOMINAL_HBM_GBS
+        roof["frac_of_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
+        roof["nominal_source"] = "GB300 HBM3e nominal bandwidth, %.0f GB/s" % NOMINAL_HBM_GBS
 
+    # The oracle timed on the host cores.  The rows it computes are also the
+    # parity check of the timed result (and of the end-to-end call's): every
+    # element of those rows against the oracle, at the parity tests' bound.
     cpu = None
+    parity = None
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
-        cpu, _ = cpu_baseline(A_cpu, B_cpu.t().contiguous() if nn else B_cpu, w,
-                              args.cpu_seconds, epi=epi)
+        cpu, rows_idx, ref_rows = cpu_baseline(A_cpu, B_cpu.t().contiguous() if nn else B_cpu, w,
+                                               args.cpu_seconds, epi=epi, bias=bias_cpu)
+        parity = parity_of_rows(C_timed[rows_idx], ref_rows, w.dtype, bool(args.out_f32))
+        parity["what"] = ("the C of the last timed step, %d whole rows (the cpu_baseline "
+                          "sample) against the fp64 oracle" % len(rows_idx))
+        if e2e is not None:
+            e2e["parity"] = parity_of_rows(hC[rows_idx], ref_rows, w.dtype, bool(args.out_f32))
 
     if rank == 0:
         line = {
@@ -631,6 +734,8 @@ def main():
             "e2e": e2e,
             "gpu_launches": args.steps * info["kernels_per_run"],
             "cpu_baseline": cpu,
+            "parity": parity,
+            "sustained": sustained,
             "step_ms_dist": dist_ms,
             "cublas_context": cublas,
         }

@@ -42,7 +42,8 @@ def test_gpu_bench_line_has_the_contract_keys():
         pytest.skip("no CUDA device")
     steps, warmup = 5, 3
     d = _run(["--workload", "gemm_4096_f16", "--steps", str(steps), "--warmup", str(warmup),
-              "--e2e-steps", "2", "--dist-reps", "0", "--cpu-seconds", "1"])
+              "--e2e-steps", "2", "--dist-reps", "0", "--cpu-seconds", "1",
+              "--sustained-seconds", "0.3"])
     _check_common(d, steps, warmup)
     assert d["scaling"] == "weak" and d["data"].startswith("synthetic")
     assert d["vs_baseline"] is None or d["vs_baseline"] > 0
@@ -68,6 +69,18 @@ def test_gpu_bench_line_has_the_contract_keys():
     assert 0 < e["value"] <= d["value"] * 1.05
     c = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
+    # the timed C and the end-to-end call's C, on the oracle's sample rows
+    p = d["parity"]
+    assert p["ok"] and p["elements"] >= 4096 and p["elements"] % 4096 == 0, p
+    assert e["parity"]["ok"] and e["parity"]["elements"] == p["elements"], e["parity"]
+    # the sustained window, with its own clock record
+    s = d["sustained"]
+    assert s["value"] > 0 and s["steps"] >= 10 and 0 < s["frac"] < 1.5
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(s["clocks"])
+    # the fractions beside the measured one
+    assert r["frac_of_nominal"] == pytest.approx(r["achieved"] / r["nominal_peak"])
+    assert r["frac_of_clock_peak"] == pytest.approx(r["achieved"] / r["clock_peak"])
+    assert r["clock_peak"] > r["nominal_peak"] * 0.8
 
 
 def test_reference_arm_times_the_oracle_on_cpu():
@@ -104,3 +117,29 @@ def test_traffic_lookup_follows_the_kernel_digest(tmp_path, monkeypatch):
                 kv = dict(x.split("=", 1) for x in line.split()[1:])
                 want = int(kv["dram_bytes_per_launch"]) if kv["source_digest"] == digest else None
                 assert bench.traffic_from_profiles(kv["workload"], digest) == want
+
+
+def test_cpu_baseline_sample_reaches_both_ends_and_checks_parity():
+    # The oracle block the bench times is the first and the last rows of the
+    # output; the same rows are the parity check of the GPU result.
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import gemm_inputs
+    import oracle
+    w = gemm_inputs.WORKLOADS["mosaic_16896x512x640_f16"]
+    A, B = gemm_inputs.make(w)
+    cpu, idx, ref = bench.cpu_baseline(A, B, w, seconds=0.05)
+    rows = len(idx)
+    assert 2 <= rows < w.M and idx[0] == 0 and idx[-1] == w.M - 1
+    assert idx == sorted(set(idx)) and ref.shape == (rows, w.N)
+    assert np.array_equal(ref, oracle.gemm_nt_entries(
+        A, B, "f16", np.repeat(idx, w.N), np.tile(np.arange(w.N), rows)).reshape(rows, w.N))
+    assert cpu["kind"] == "oracle" and "first" in cpu["sample"] and "last" in cpu["sample"]
+    C = torch.from_numpy(oracle.round_to(ref, "f16").view(np.int16)).view(torch.float16)
+    assert bench.parity_of_rows(C, ref, "f16", False)["ok"]
+    bad = C.clone()
+    bad[rows - 1, 7] = float(bad[rows - 1, 7]) + 0.5
+    st = bench.parity_of_rows(bad, ref, "f16", False)
+    assert not st["ok"] and st["bad"] == 1

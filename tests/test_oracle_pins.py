@@ -424,3 +424,27 @@ def test_no_bias_is_a_zero_bias():
     A, B = gemm_inputs.custom(5, 6, 16, seed=23)   # M < N (see test_bias_alone_with_zero_a)
     z = torch.zeros(6, dtype=torch.float16)
     assert np.array_equal(oracle.gemm_nt(A, B, "f16", bias=z), oracle.gemm_nt(A, B, "f16"))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_row_block_comparison_equals_whole_matrix_comparison(dtype):
+    # The full-size parity tests compare 8192 x 8192 results a block of rows
+    # at a time; the blocks must add up to exactly the whole-matrix verdict,
+    # including a planted element error in the last, partial block.
+    A, B = gemm_inputs.custom(203, 96, 300, dtype=dtype, dist="normal_scaled", seed=14)
+    ref = oracle.gemm_nt(A, B, dtype)
+    rnd = oracle.decode(oracle.round_to(ref, dtype), dtype)
+    noisy = rnd + 0.4 * tolerance.ulp(ref, dtype) * np.sign(np.sin(np.arange(ref.size))).reshape(ref.shape)
+    for got in (rnd, noisy):
+        whole = tolerance.compare(got, ref, dtype)
+        blocks = tolerance.compare_rows(lambda r0, r1: got[r0:r1], ref, dtype, chunk=64)
+        assert blocks["ok"] == whole["ok"] and blocks["bad"] == whole["bad"]
+        for key in ("frob", "frob_vs_exact", "max_abs", "max_ulp"):
+            assert blocks[key] == pytest.approx(whole[key], rel=1e-12, abs=1e-300), key
+    bad = rnd.copy()
+    bad[200, 5] = ref[200, 5] + 3 * tolerance.ulp(ref[200, 5], dtype) + 1.001e-3
+    blocks = tolerance.compare_rows(lambda r0, r1: bad[r0:r1], ref, dtype, chunk=64)
+    assert not blocks["ok"] and blocks["bad"] == 1 and blocks["first_bad"] == (200, 5)
+    bad[3, 3] = np.nan
+    blocks = tolerance.compare_rows(lambda r0, r1: bad[r0:r1], ref, dtype, chunk=64)
+    assert blocks["bad"] == 2 and blocks["first_bad"] == (3, 3) and not blocks["ok"]

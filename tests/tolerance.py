@@ -66,3 +66,51 @@ def compare(got, ref, dtype: str, ulps: float = ULPS, abs_tol: float = ABS):
         "bad": int(bad.sum()),
         "first_bad": (tuple(int(i) for i in np.argwhere(bad)[0]) if bad.any() else None),
     }
+
+
+def compare_rows(got_rows, ref, dtype: str, chunk: int = 512, ulps: float = ULPS,
+                 abs_tol: float = ABS):
+    """compare() over a large matrix, a block of `chunk` rows at a time.
+
+    got_rows(r0, r1) returns the decoded GPU rows [r0, r1) as float64; ref is
+    the oracle's full fp64 result.  The per-element bound and the Frobenius
+    norms are the ones compare() uses; the norms are accumulated as sums of
+    squares over the blocks, so no temporary larger than one block exists."""
+    r = np.asarray(ref)
+    M = r.shape[0]
+    bad = 0
+    first_bad = None
+    max_abs = max_ulp = 0.0
+    num = num_exact = den = 0.0
+    for r0 in range(0, M, chunk):
+        r1 = min(M, r0 + chunk)
+        g = np.asarray(got_rows(r0, r1), dtype=np.float64)
+        rr = np.asarray(r[r0:r1], dtype=np.float64)
+        assert g.shape == rr.shape, (g.shape, rr.shape)
+        finite = np.isfinite(g)
+        err = np.where(finite, np.abs(g - rr), np.inf)
+        u = ulp(rr, dtype)
+        b = (~finite) | (err > ulps * u + abs_tol)
+        if b.any():
+            bad += int(b.sum())
+            if first_bad is None:
+                i, j = np.argwhere(b)[0]
+                first_bad = (int(i) + r0, int(j))
+        max_abs = max(max_abs, float(err.max()) if err.size else 0.0)
+        max_ulp = max(max_ulp, float((err / u).max()) if err.size else 0.0)
+        base = rr if dtype in ("f16", "f32") else rounded_reference(rr, dtype)
+        num += float(np.sum(np.where(finite, g - base, np.inf) ** 2))
+        num_exact += float(np.sum(np.where(finite, g - rr, np.inf) ** 2))
+        den += float(np.sum(rr * rr))
+    nr = np.sqrt(den)
+    frob = float(np.sqrt(num) / nr) if nr > 0 else float(np.sqrt(num))
+    return {
+        "ok": bool(bad == 0 and frob <= FROB),
+        "frob_vs_exact": float(np.sqrt(num_exact) / nr) if nr > 0 else 0.0,
+        "max_abs": max_abs,
+        "max_ulp": max_ulp,
+        "frob": frob,
+        "bad": bad,
+        "first_bad": first_bad,
+        "elements": int(r.size),
+    }
