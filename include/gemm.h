@@ -76,7 +76,10 @@ typedef enum {
   GEMM_ERR_SMEM_BUDGET = 3,   /* requested stages/tile do not fit the shared-memory budget */
   GEMM_ERR_PLAN_MISMATCH = 4, /* run arguments differ from the plan's */
   GEMM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
-  GEMM_ERR_TIMEOUT = 6        /* device: a pipeline wait exceeded its time limit */
+  GEMM_ERR_TIMEOUT = 6,       /* device: a pipeline wait exceeded its time limit */
+  GEMM_ERR_BOUNDS = 7         /* device, bounds-checked build only: an index or copy
+                                 coordinate failed its range check (the access was
+                                 skipped; see gemm_check_t) */
 } gemm_status_t;
 
 typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1 } gemm_dtype_t;
@@ -117,7 +120,12 @@ typedef struct {
   int debug_fault;     /* test hook, 0 in normal use.  1: the first CTA's copy engine
                           never receives its first K slice, so the pipeline's waits run
                           out their time limit and gemm_plan_check reports
-                          GEMM_ERR_TIMEOUT (every other tile still completes) */
+                          GEMM_ERR_TIMEOUT (every other tile still completes).
+                          2 (bounds-checked build only; GEMM_ERR_INVALID_ARG in the
+                          normal build): the range check of the first CTA's first copy
+                          is made to fail -- its coordinates are valid -- so the copy is
+                          skipped and gemm_plan_check reports GEMM_ERR_BOUNDS with
+                          GEMM_CHECK_TMA_COORD */
   int k_serpentine;    /* K order of successive waves of tiles: 0 = auto (alternate when
                           the A and B rows one wave of tiles reads exceed half of L2),
                           1 = alternate (a CTA's odd-numbered tiles walk K downwards, so
@@ -246,6 +254,39 @@ typedef enum {
   GEMM_WAIT_SK_FREE = (3 << 16) | 4         /* cluster split: the owner's ring to be free */
 } gemm_wait_t;
 
+/* Bounds-checked build.  The library can be compiled with
+ * -DSPGEMM_BOUNDS_CHECKS=1 (the Python package builds it as
+ * libspgemm_checked.so next to libspgemm.so).  Its kernels check, before each
+ * access, the indexes and coordinates they derive: tile indexes, K slots and
+ * copy coordinates (the K coordinate of a tiled copy must be 16-byte
+ * aligned), TMEM columns, ring slots, staging buffers, C blocks and stream-K
+ * workspace slots.  A failed check records GEMM_ERR_BOUNDS with the check's
+ * identity (below) as the detail, skips the access and ends that role; the
+ * other roles' bounded waits then run out, the kernel exits and the GPU stays
+ * usable -- nothing traps.  This guards the shared-memory ring the Mosaic
+ * GPU pipelining guide's delay_release discussion is about: a slot index or
+ * coordinate that went wrong is reported instead of corrupting memory.  The
+ * checks cost time; the normal build compiles them out.
+ * Detail codes: role << 16 | 16 + id, role 0 = kernel set-up, 1 = TMA
+ * producer, 2 = MMA issuer, 3 = epilogue. */
+typedef enum {
+  GEMM_CHECK_SMEM_LAYOUT = (0 << 16) | 16, /* ring + staging + barriers exceed the launch's
+                                              shared memory */
+  GEMM_CHECK_TILE = (1 << 16) | 16,        /* a unit's tile index or tile coordinates */
+  GEMM_CHECK_K_SLICE = (1 << 16) | 17,     /* a K slot outside the unit's range or K */
+  GEMM_CHECK_TMA_COORD = (1 << 16) | 18,   /* a copy coordinate out of range or unaligned */
+  GEMM_CHECK_MMA_TMEM = (2 << 16) | 16,    /* accumulator columns beyond the TMEM allocation */
+  GEMM_CHECK_MMA_SLOT = (2 << 16) | 17,    /* a ring slot index beyond the ring */
+  GEMM_CHECK_EPI_TMEM = (3 << 16) | 16,    /* TMEM columns read beyond the allocation */
+  GEMM_CHECK_STAGING = (3 << 16) | 17,     /* a staging buffer beyond the warp's area */
+  GEMM_CHECK_STORE = (3 << 16) | 18,       /* a C block outside the tile grid or unaligned */
+  GEMM_CHECK_PARTIAL = (3 << 16) | 19,     /* a stream-K workspace slot beyond the workspace */
+  GEMM_CHECK_FIXUP = (3 << 16) | 20        /* a partial's shared-memory region beyond the ring */
+} gemm_check_t;
+
+/* 1 when this library is the bounds-checked build, 0 otherwise. */
+int gemm_bounds_checked(void);
+
 /* Synchronise the plan's device and read (then clear) its device status word.
  * *device_status receives GEMM_OK or the code a kernel recorded (e.g.
  * GEMM_ERR_TIMEOUT); *detail (may be NULL) receives the place it was recorded
@@ -296,8 +337,10 @@ void gemm_plan_destroy(gemm_plan_t* plan);
 /* Static text for a status code ("GEMM_OK", ...). */
 const char* gemm_status_string(gemm_status_t s);
 
-/* Static text for the detail of a device status word ("MMA issuer waiting
- * for a ring slot's copies", ...); "" for 0, "unknown wait" otherwise. */
+/* Static text for the detail of a device status word: a gemm_wait_t ("MMA
+ * issuer waiting for a ring slot's copies", ...) or a gemm_check_t ("copy
+ * coordinate out of range or unaligned", ...); "" for 0, "unknown wait"
+ * otherwise. */
 const char* gemm_wait_detail_string(int32_t detail);
 
 /* Last error message recorded by this host thread (argument that failed,
@@ -340,7 +383,8 @@ const char* gemm_version(void);
  * The first call on each device sets that device up (takes the device
  * address of the static array with cudaGetSymbolAddress, sets the kernels'
  * shared-memory limits, looks up the tensor-map encoder).  Make that first
- * call before any stream capture.  Every call on a device shares the one
+ * call before any stream capture.  A set-up that fails is not kept: the
+ * call returns its error and the next call on that device tries again.  Every call on a device shares the one
  * array and leaves its contents behind (the status words are cleared at the
  * start of each call): calls whose work overlaps on the GPU -- on different
  * streams, or from different host threads -- race on it. */

@@ -11,6 +11,12 @@ memory and the current stream only.
 There is no fallback: if the library is missing or cannot be loaded, every
 call raises.
 
+With the environment variable ``SPGEMM_BOUNDS_CHECKS=1`` the package loads
+the bounds-checked build ``_lib/libspgemm_checked.so`` instead (built on
+first use): its kernels range-check their indexes and copy coordinates and
+report a failed check as ``GEMM_ERR_BOUNDS`` (see ``gemm_check_t`` in
+``include/gemm.h``).
+
 Convenience layer: :func:`matmul_nt` takes torch CUDA tensors A (M,K) and
 B (N,K), caches a plan per problem, and launches on the current stream --
 the operation of the TileLang tutorial's ``matmul_auto`` (A (M,K), B (N,K),
@@ -37,7 +43,8 @@ __all__ = [
     "gemm_device_query", "gemm_plan_describe", "GemmDeviceDesc", "describe", "GB300",
     "get_plan", "set_plan_cache_limit", "clear_plan_cache", "plan_cache_size",
     "GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED", "GEMM_ERR_SMEM_BUDGET",
-    "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT",
+    "GEMM_ERR_PLAN_MISMATCH", "GEMM_ERR_CUDA", "GEMM_ERR_TIMEOUT", "GEMM_ERR_BOUNDS",
+    "gemm_bounds_checked", "bounds_checked_requested",
     "GEMM_F16", "GEMM_BF16", "GEMM_EPI_NONE", "GEMM_EPI_GELU_TANH", "GEMM_EPI_RELU",
     "GEMM_PIPELINED", "GEMM_SINGLE_BUFFER",
 ]
@@ -52,6 +59,7 @@ GEMM_ERR_SMEM_BUDGET = 3
 GEMM_ERR_PLAN_MISMATCH = 4
 GEMM_ERR_CUDA = 5
 GEMM_ERR_TIMEOUT = 6
+GEMM_ERR_BOUNDS = 7
 
 GEMM_F16 = 0
 GEMM_BF16 = 1
@@ -114,8 +122,14 @@ _lib = None
 _lib_lock = threading.Lock()
 
 
+def bounds_checked_requested() -> bool:
+    """True when SPGEMM_BOUNDS_CHECKS=1 asks for the bounds-checked build."""
+    return os.environ.get("SPGEMM_BOUNDS_CHECKS", "0") not in ("", "0")
+
+
 def library_path() -> str:
-    return _LIB_PATH
+    from . import _build
+    return _build.LIB_CHECKED if bounds_checked_requested() else _LIB_PATH
 
 
 def load_library(path: Optional[str] = None):
@@ -126,9 +140,10 @@ def load_library(path: Optional[str] = None):
             return _lib
         if path is None:
             from . import _build
-            if not _build.up_to_date():
-                _build.build()
-            path = _LIB_PATH
+            checked = bounds_checked_requested()
+            if not _build.up_to_date(checked):
+                _build.build(checked=checked)
+            path = library_path()
         if not os.path.exists(path):
             raise ImportError("libspgemm.so not found at %s; run __graft_entry__.build()" % path)
         lib = ctypes.CDLL(path)
@@ -162,6 +177,8 @@ def load_library(path: Optional[str] = None):
         lib.gemm_smem_bytes.restype = ctypes.c_size_t
         lib.gemm_version.argtypes = []
         lib.gemm_version.restype = ctypes.c_char_p
+        lib.gemm_bounds_checked.argtypes = []
+        lib.gemm_bounds_checked.restype = ci
         lib.gemm_run_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, vp]
         lib.gemm_run_noalloc.restype = ci
         lib.gemm_device_query.argtypes = [ci, ctypes.POINTER(GemmDeviceDesc)]
@@ -203,6 +220,11 @@ def gemm_last_error() -> str:
 
 def gemm_version() -> str:
     return load_library().gemm_version().decode()
+
+
+def gemm_bounds_checked() -> int:
+    """1 when the loaded library is the bounds-checked build."""
+    return int(load_library().gemm_bounds_checked())
 
 
 def gemm_smem_bytes(bm: int, bn: int, bk: int, elem_bytes: int, stages: int) -> int:

@@ -290,6 +290,7 @@ const char* gemm_status_string(gemm_status_t s) {
     case GEMM_ERR_PLAN_MISMATCH: return "GEMM_ERR_PLAN_MISMATCH";
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_BOUNDS: return "GEMM_ERR_BOUNDS";
   }
   return "GEMM_ERR_UNKNOWN";
 }
@@ -301,6 +302,16 @@ static_assert(GEMM_WAIT_PRODUCER_EMPTY == kDetailProducerEmpty &&
                   GEMM_WAIT_SK_FLAG == kDetailSkFlag && GEMM_WAIT_SK_COPY == kDetailSkCopy &&
                   GEMM_WAIT_SK_FREE == kDetailSkFree,
               "gemm_wait_t must match the kernel's wait identifiers");
+static_assert(GEMM_ERR_BOUNDS == kStatusBounds && GEMM_ERR_TIMEOUT == kStatusTimeout &&
+                  GEMM_CHECK_SMEM_LAYOUT == kCheckSmemLayout && GEMM_CHECK_TILE == kCheckTile &&
+                  GEMM_CHECK_K_SLICE == kCheckKSlice && GEMM_CHECK_TMA_COORD == kCheckTmaCoord &&
+                  GEMM_CHECK_MMA_TMEM == kCheckMmaTmem && GEMM_CHECK_MMA_SLOT == kCheckMmaSlot &&
+                  GEMM_CHECK_EPI_TMEM == kCheckEpiTmem && GEMM_CHECK_STAGING == kCheckStaging &&
+                  GEMM_CHECK_STORE == kCheckStore && GEMM_CHECK_PARTIAL == kCheckPartial &&
+                  GEMM_CHECK_FIXUP == kCheckFixup,
+              "gemm_check_t must match the kernel's check identifiers");
+
+int gemm_bounds_checked(void) { return SPGEMM_BOUNDS_CHECKS ? 1 : 0; }
 
 const char* gemm_wait_detail_string(int32_t detail) {
   switch (detail) {
@@ -314,6 +325,17 @@ const char* gemm_wait_detail_string(int32_t detail) {
     case GEMM_WAIT_SK_FLAG: return "stream-K owner waiting for its partner's partial";
     case GEMM_WAIT_SK_COPY: return "stream-K owner waiting for the partial's bytes";
     case GEMM_WAIT_SK_FREE: return "cluster split contributor waiting for the owner's ring";
+    case GEMM_CHECK_SMEM_LAYOUT: return "ring, staging and barriers exceed the launch's shared memory";
+    case GEMM_CHECK_TILE: return "tile index or tile coordinates out of range";
+    case GEMM_CHECK_K_SLICE: return "K slot outside the unit's range or the K extent";
+    case GEMM_CHECK_TMA_COORD: return "copy coordinate out of range or unaligned";
+    case GEMM_CHECK_MMA_TMEM: return "accumulator columns beyond the TMEM allocation";
+    case GEMM_CHECK_MMA_SLOT: return "ring slot index beyond the ring";
+    case GEMM_CHECK_EPI_TMEM: return "epilogue TMEM columns beyond the allocation";
+    case GEMM_CHECK_STAGING: return "staging buffer beyond the warp's staging area";
+    case GEMM_CHECK_STORE: return "C block outside the tile grid or unaligned";
+    case GEMM_CHECK_PARTIAL: return "stream-K workspace slot beyond the workspace";
+    case GEMM_CHECK_FIXUP: return "stream-K partial region beyond the ring";
   }
   return "unknown wait";
 }
@@ -365,8 +387,12 @@ gemm_status_t check_create_args(int64_t M, int64_t N, int64_t K, gemm_dtype_t dt
     if (w->group < 0 || w->ctas < 0)
       return fail(GEMM_ERR_INVALID_ARG, "negative raster_group / max_ctas");
     if (tuning->timeout_ns < 0) return fail(GEMM_ERR_INVALID_ARG, "negative timeout_ns");
-    if (tuning->debug_fault < 0 || tuning->debug_fault > 1)
-      return fail(GEMM_ERR_INVALID_ARG, "debug_fault %d not in {0, 1}", tuning->debug_fault);
+    if (tuning->debug_fault < 0 || tuning->debug_fault > 2)
+      return fail(GEMM_ERR_INVALID_ARG, "debug_fault %d not in {0, 1, 2}", tuning->debug_fault);
+    if (tuning->debug_fault == 2 && !SPGEMM_BOUNDS_CHECKS)
+      return fail(GEMM_ERR_INVALID_ARG,
+                  "debug_fault 2 forces a range check to fail; only the bounds-checked build "
+                  "has the checks");
     if (tuning->out_f32 < 0 || tuning->out_f32 > 1)
       return fail(GEMM_ERR_INVALID_ARG, "out_f32 %d not in {0, 1}", tuning->out_f32);
     if (tuning->b_kn < 0 || tuning->b_kn > 1)
@@ -980,6 +1006,9 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.sk_tiles = static_cast<int>(plan->sk_tiles);
   prm.sk_ws = plan->sk_ws;
   prm.sk_flags = plan->sk_flags;
+  prm.sk_slots = plan->sk_tiles > 0
+                     ? static_cast<int>(plan->sk_tiles * plan->cg * 4 * plan->epi_groups)
+                     : 0;
   prm.bias = bias;
 
   cudaError_t e = launch(plan->bn, plan->cg, plan->tmA, plan->tmB, plan->tmBt, plan->tmC,

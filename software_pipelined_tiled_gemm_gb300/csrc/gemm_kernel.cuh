@@ -68,6 +68,20 @@ static __device__ __noinline__ void record_error(int* status, int code, int deta
   if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, detail);
 }
 
+// Range checks of the bounds-checked build (compiled with
+// SPGEMM_BOUNDS_CHECKS=1).  SPGEMM_OUT_OF_BOUNDS(cond, p, what) is true when
+// `cond` fails; it then records GEMM_ERR_BOUNDS and the check's identity
+// `what` in the status word, the caller skips the access and ends its role,
+// and the other roles' bounded waits run out -- no trap, the GPU stays
+// usable.  In the normal build it is the constant false and `cond` is not
+// evaluated.
+__device__ __forceinline__ bool check_failed(const Params& p, int what) {
+  record_error(p.status, kStatusBounds, what);
+  return true;
+}
+#define SPGEMM_OUT_OF_BOUNDS(cond, p, what) \
+  (SPGEMM_BOUNDS_CHECKS && !(cond) && ::spgemm::check_failed((p), (what)))
+
 // Suspend-time hint of the long waits (an epilogue warp waits for most of a
 // tile's main loop): wake on the phase, not on a short default limit.
 constexpr uint32_t kLongWaitHintNs = 1000000u;
@@ -363,6 +377,15 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
   uint8_t* staging = smem + ring_bytes;
   const uint32_t staging_bytes = 4u * epi_groups * p.store_bufs * kStoreBuf;
   const uint32_t bar_base = sbase + ring_bytes + staging_bytes;
+  // Ring, staging, barriers and the TMEM address slot inside the launch's
+  // dynamic shared memory (every thread of every CTA decides alike, so all
+  // leave before any barrier, TMEM allocation or cluster synchronisation).
+  if (SPGEMM_OUT_OF_BOUNDS(S >= 1 && S <= kMaxStages && p.store_bufs >= 1 && p.store_bufs <= 2 &&
+                               (sbase - raw_addr) + ring_bytes + staging_bytes +
+                                       8u * (2 * kMaxStages + 5 + 2 * kEpiWarps) + 4u <=
+                                   ptx::dynamic_smem_bytes(),
+                           p, kCheckSmemLayout))
+    return;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (kMaxStages + s); };
   auto tfull_bar = [&](int a) { return bar_base + 8u * (2 * kMaxStages + a); };
@@ -468,6 +491,13 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
       while (ok && it.next(p, x)) {
         int mb, nb;
         tile_coords(x.tile, p, mb, nb);
+        if (SPGEMM_OUT_OF_BOUNDS(x.tile >= 0 && x.tile < p.num_tiles && mb >= 0 && mb < p.tiles_m &&
+                                     nb >= 0 && nb < p.tiles_n,
+                                 p, kCheckTile) ||
+            SPGEMM_OUT_OF_BOUNDS(x.k0 >= 0 && x.k0 < x.k1 && x.k1 <= p.k_blocks, p, kCheckKSlice)) {
+          ok = false;
+          break;
+        }
         const bool narrow = kSplit && x.sub >= 0;
         const int n_width = narrow ? BN / p.tail_splits : BN;   // columns of this unit
         const int b_rows = n_width / CG;                        // B rows this CTA loads
@@ -494,8 +524,25 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             if (pk >= x.k0 && pk < x.k1) ptx::tma_prefetch_l2_2d(&tmBp, pk * kBK, b_row);
           }
           const uint32_t sa = sbase + stage * kStage;
+          // Copy coordinates: the K slot inside the unit's range, the first K
+          // element 16-byte aligned (x of a tiled copy) and inside the K
+          // extent, the rows inside the tile grid.  Test hook 2 makes this
+          // check fail for CTA 0's first copy (its coordinates are valid).
+          {
+            const int kx_first = kb * kSub * kBK, kx_last = (kb * kSub + kSub - 1) * kBK;
+            const bool forced = p.inject_fault == 2 && blockIdx.x == 0 && x.seq == 0 && i == 0;
+            if (SPGEMM_OUT_OF_BOUNDS(kb >= x.k0 && kb < x.k1 && stage < S, p, kCheckKSlice) ||
+                SPGEMM_OUT_OF_BOUNDS(!forced && kx_first >= 0 && (kx_first & 7) == 0 &&
+                                         kx_last < p.k_blocks * kSub * kBK && a_row >= 0 &&
+                                         a_row < p.tiles_m * kTileM && b_row >= 0 &&
+                                         b_row < p.tiles_n * BN && (!kKN || (b_row & 63) == 0),
+                                     p, kCheckTmaCoord)) {
+              ok = false;
+              break;
+            }
+          }
           // Test hook: the first slice of CTA 0 is announced but never copied.
-          const bool skip = p.inject_fault && blockIdx.x == 0 && x.seq == 0 && i == 0;
+          const bool skip = p.inject_fault == 1 && blockIdx.x == 0 && x.seq == 0 && i == 0;
           if constexpr (CG == 2) {
             // Both CTAs' copies count on the leader's full barrier; only the
             // leader announces the bytes (of both CTAs).
@@ -564,10 +611,14 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
         if (!wait_bounded_cluster<CG>(tempty_bar(acc), acc_phase ^ 1u, p, kDetailMmaAccEmpty))
           break;
         ptx::tc_fence_after_sync();
+        if (SPGEMM_OUT_OF_BOUNDS(acc >= 0 && acc < p.num_acc && (acc + 1) * BN <= p.tmem_cols, p,
+                                 kCheckMmaTmem))
+          break;
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         const int nk = x.k1 - x.k0;
         for (int kb = 0; kb < nk; ++kb) {  // iteration count (slices may be rotated)
-          if (!wait_bounded(full_bar(stage), phase, p, kDetailMmaFull)) {
+          if (!wait_bounded(full_bar(stage), phase, p, kDetailMmaFull) ||
+              SPGEMM_OUT_OF_BOUNDS(stage >= 0 && stage < S, p, kCheckMmaSlot)) {
             ok = false;
             break;
           }
@@ -671,6 +722,21 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
       float* partial = (kSplit && x.role != kWhole)
                            ? p.sk_ws + static_cast<size_t>(flag_idx) * (warp_partial / 4u)
                            : nullptr;
+      // TMEM columns, staging buffers, the C block, and (stream-K) the
+      // partial's workspace slot and its shared-memory region.
+      if (SPGEMM_OUT_OF_BOUNDS(acc >= 0 && acc < p.num_acc && c_hi <= BN &&
+                                   (acc + 1) * BN <= p.tmem_cols,
+                               p, kCheckEpiTmem) ||
+          SPGEMM_OUT_OF_BOUNDS((ew + 1) * p.store_bufs * kStoreBuf <= staging_bytes, p,
+                               kCheckStaging) ||
+          SPGEMM_OUT_OF_BOUNDS(row0 >= 0 && row0 < p.tiles_m * kTileM && n0 >= 0 && (n0 & 63) == 0,
+                               p, kCheckStore) ||
+          SPGEMM_OUT_OF_BOUNDS(!kSplit || x.role == kWhole || p.sk_cluster ||
+                                   (static_cast<int>(flag_idx) < p.sk_slots && p.sk_ws != nullptr),
+                               p, kCheckPartial) ||
+          SPGEMM_OUT_OF_BOUNDS(!kSplit || x.role == kWhole || (ew + 1) * warp_partial <= ring_bytes,
+                               p, kCheckFixup))
+        break;
       bool have_partial = false;
       if (kSplit && x.role == kContrib && p.sk_cluster) {
         // Cluster split: stage this warp's partial in this CTA's own idle

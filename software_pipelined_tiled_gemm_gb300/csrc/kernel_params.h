@@ -5,6 +5,12 @@
 #include <cstddef>
 #include <cstdint>
 
+// 1 in the bounds-checked build (device-side range checks that record
+// GEMM_ERR_BOUNDS instead of making the access), 0 in the normal build.
+#ifndef SPGEMM_BOUNDS_CHECKS
+#define SPGEMM_BOUNDS_CHECKS 0
+#endif
+
 namespace spgemm {
 
 constexpr int kBM = 128;          // CTA tile rows (one TMEM lane per row)
@@ -25,6 +31,7 @@ constexpr uint32_t kBarrierBytes = 8u * (2 * kMaxStages + 5 + 2 * kEpiWarps) + 1
 constexpr uint32_t kAlignSlack = 1024u;
 
 constexpr int kStatusTimeout = 6;  // == GEMM_ERR_TIMEOUT
+constexpr int kStatusBounds = 7;   // == GEMM_ERR_BOUNDS (bounds-checked build)
 
 constexpr int kMaxTailSplits = 4;     // narrow tiles a tail tile may be cut into (N >= 64 each)
 constexpr int kPrefetchSlices = 4;    // K slices per L2 prefetch box (4 x 128 B per row)
@@ -40,6 +47,19 @@ constexpr int kDetailEpiFull = (3 << 16) | 1;
 constexpr int kDetailSkFlag = (3 << 16) | 2;
 constexpr int kDetailSkCopy = (3 << 16) | 3;
 constexpr int kDetailSkFree = (3 << 16) | 4;
+// Which range check failed (status word [1] with kStatusBounds): role << 16 |
+// 16 + check id (the bounds-checked build only).
+constexpr int kCheckSmemLayout = (0 << 16) | 16;  // ring + staging + barriers exceed the launch's smem
+constexpr int kCheckTile = (1 << 16) | 16;        // unit's tile index or tile coordinates
+constexpr int kCheckKSlice = (1 << 16) | 17;      // K slot outside the unit's range or the K extent
+constexpr int kCheckTmaCoord = (1 << 16) | 18;    // copy coordinate out of range or not 16-byte aligned
+constexpr int kCheckMmaTmem = (2 << 16) | 16;     // accumulator columns beyond the TMEM allocation
+constexpr int kCheckMmaSlot = (2 << 16) | 17;     // ring slot index beyond the ring
+constexpr int kCheckEpiTmem = (3 << 16) | 16;     // TMEM columns read beyond the allocation
+constexpr int kCheckStaging = (3 << 16) | 17;     // staging buffer beyond the warp's staging area
+constexpr int kCheckStore = (3 << 16) | 18;       // C store outside the tile grid or unaligned
+constexpr int kCheckPartial = (3 << 16) | 19;     // stream-K partial / flag index beyond the workspace
+constexpr int kCheckFixup = (3 << 16) | 20;       // partial's shared-memory region beyond the ring
 
 struct Params {
   int M, N;              // output extent
@@ -80,6 +100,7 @@ struct Params {
   int sk_tiles;
   float* sk_ws;
   int* sk_flags;
+  int sk_slots;          // epilogue-warp partials (and flags) sk_ws / sk_flags hold
   // 1: each unit starts its K loop at a different slice (wrapping around),
   // so CTAs that share the same A rows do not all read the same A slice at
   // the same time (used when a single row of tiles spans the whole grid).
@@ -123,7 +144,9 @@ struct Params {
   // accumulator before the epilogue function; nullptr for none.
   const void* bias;
   // Test hook: 1 = the producer of CTA 0 announces but never issues the
-  // copies of its first K slice (see gemm_tuning_t::debug_fault).
+  // copies of its first K slice; 2 = (bounds-checked build) the range check
+  // of that copy is made to fail, the coordinates themselves being valid
+  // (see gemm_tuning_t::debug_fault).
   int inject_fault;
 };
 

@@ -24,7 +24,6 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
-#include <functional>
 #include <mutex>
 
 #include "../../include/gemm.h"
@@ -53,7 +52,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 struct DeviceSetup {
-  std::once_flag once;
+  std::mutex mu;
+  bool done = false;           // set only by a set-up that succeeded
   cudaError_t err = cudaSuccess;
   gemm_status_t status = GEMM_OK;
   uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
@@ -65,7 +65,9 @@ struct DeviceSetup {
 DeviceSetup g_setup[kMaxDevices];
 
 void setup_device(DeviceSetup& s, int dev) {
-  // Runs once per device, with `dev` current.
+  // Runs with `dev` current, until it succeeds once on that device.
+  s.status = GEMM_OK;
+  s.err = cudaSuccess;
   cudaDeviceProp prop;
   s.err = cudaGetDeviceProperties(&prop, dev);
   if (s.err != cudaSuccess) { s.status = GEMM_ERR_CUDA; return; }
@@ -147,8 +149,17 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
   if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
   DeviceSetup& s = g_setup[dev];
-  std::call_once(s.once, setup_device, std::ref(s), dev);
-  if (s.status != GEMM_OK) return s.status;
+  {
+    // A failed set-up is not kept: the next call on this device tries again
+    // (the failure may have been transient, e.g. an error left over from
+    // earlier work, or a first call made during a stream capture).
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (!s.done) {
+      setup_device(s, dev);
+      if (s.status != GEMM_OK) return s.status;
+      s.done = true;
+    }
+  }
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_handle);
   if (K == 0) return cudaMemsetAsync(C, 0, bytesC, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

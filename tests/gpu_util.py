@@ -43,7 +43,9 @@ def run_device(A: torch.Tensor, B: torch.Tensor, dtype: str, epilogue=None, stag
     if bias is not None:
         _, bd = place(bias, 0)
         bias_ptr = bd.data_ptr()
-    cbuf = torch.empty(M * N + c_offset + 64, dtype=_TD[dtype], device=dev)
+    # C holds the input type, or fp32 for a plan with out_f32.
+    c_dtype = torch.float32 if tuning.get("out_f32") else _TD[dtype]
+    cbuf = torch.empty(M * N + c_offset + 64, dtype=c_dtype, device=dev)
     cbuf.view(torch.int16).fill_(np.int16(np.uint16(fill).view(np.int16)).item())
     c = cbuf[c_offset:c_offset + M * N]
     plan = sg.Plan(M, N, K, dtype, epilogue, stages, variant, 0, **tuning)
