@@ -75,6 +75,10 @@ def parse():
     ap.add_argument("--no-cublas", action="store_true",
                     help="skip the torch.matmul (cuBLAS) context timing")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
+                    help="skip the compact measurements of the other configurations")
+    ap.add_argument("--other-steps", type=int, default=20,
+                    help="timed steps of each other configuration")
     ap.add_argument("--sustained-seconds", type=float, default=1.5,
                     help="length of the back-to-back sustained window (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -423,6 +427,90 @@ def run_reference(args, w, ws, rank):
     return 0
 
 
+# The other configurations reported beside the headline in one run: the
+# workloads the GEMM is specified on, plus the single-buffer contrast.
+OTHER_CONFIGS = [("gemm_256_f16", "pipelined"), ("gemm_4096_f16", "pipelined"),
+                 ("gemm_8192_f16", "single_buffer"), ("gelu_3072x16384x4096_bf16", "pipelined"),
+                 ("ragged_4095x4097x8191_f16", "pipelined"), ("skinny_64x8192x8192_f16", "pipelined")]
+
+
+def measure_config(sg, torch, dev, stream, w, variant, stages, steps, warmup, peaks, peak_src,
+                   scrub):
+    """A compact measurement of one configuration with the headline's
+    protocol: inputs resident, `warmup` untimed steps, then `steps` steps back
+    to back between two events on the launch stream, or -- when the operands
+    fit in L2 -- each step after an L2 flush, bracketed by its own events.
+    Reports TFLOP/s, the roofline of its bound and torch.matmul on the same
+    operands as context."""
+    epi = None if w.epilogue == "none" else w.epilogue
+    if variant == "single_buffer":
+        stages = 1
+    A, B = gemm_inputs.make(w)
+    a, b = A.to(dev), B.to(dev)
+    c = torch.empty(w.M, w.N, dtype=a.dtype, device=dev)
+    plan = sg.Plan(w.M, w.N, w.K, w.dtype, epi, stages, variant, dev.index)
+    sptr = stream.cuda_stream
+    operand_bytes = (w.M * w.K + w.N * w.K) * 2
+    flush = operand_bytes <= L2_BYTES
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(max(warmup, 3)):
+                fn()
+            if not flush:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                return e0.elapsed_time(e1) / n
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for e0, e1 in evs:
+                scrub.fill_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
+
+    try:
+        ms = timed(lambda: plan.run_ptr(a.data_ptr(), b.data_ptr(), c.data_ptr(), sptr), steps)
+        ds, detail = plan.check()
+        if ds != 0:
+            raise SystemExit("device status %d (detail %#x) in %s" % (ds, detail, w.name))
+        info = plan.info()
+    finally:
+        plan.close()
+    flops = 2.0 * w.M * w.N * w.K
+    min_bytes = 2.0 * (w.M * w.K + w.N * w.K + w.M * w.N)
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_TFLOPS))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM))
+    out = {"variant": variant, "stages": info["stages"], "value": tflops, "unit": UNIT,
+           "ms_per_step": ms, "steps": steps, "kernels_per_step": info["kernels_per_run"],
+           "l2": "flushed before every step" if flush else "operands larger than L2; no flush",
+           "plan": "%dx%d tiles, cta_group %d, %d slice(s) per slot, %s" % (
+               info["tile_m"], info["tile_n"], info["cta_group"], info["k_sub"],
+               "stream-K tail" if info["stream_k"] else
+               ("narrow tail tiles" if info["tail_splits"] > 1 else "whole tiles"))}
+    if flops / min_bytes < peak * 1e12 / (hbm * 1e9):
+        out["roofline"] = {"bound": "hbm", "achieved": min_bytes / (ms * 1e-3) / 1e9, "peak": hbm,
+                           "unit": "GB/s", "peak_source": "%s hbm_gbs" % peak_src}
+    else:
+        out["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": UNIT,
+                           "peak_source": "%s bf16_tflops" % peak_src}
+    out["roofline"]["frac"] = out["roofline"]["achieved"] / out["roofline"]["peak"]
+    if epi is None and variant == "pipelined":
+        bt = b.t()
+        cms = timed(lambda: torch.matmul(a, bt), steps)
+        out["cublas_context"] = {"ms": cms, "tflops": flops / (cms * 1e-3) / 1e12}
+    del a, b, c
+    return out
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
@@ -645,6 +733,18 @@ def main():
             sustained["frac_of_pipe_at_clock"] = (
                 sus_val / ws / (info["sm_count"] * TENSOR_FLOP_PER_SM_CYCLE * mhz * 1e6 / 1e12))
 
+    # The other configurations, measured in the same run (single GPU only).
+    others = None
+    if args.other_configs and ws == 1 and args.workload == "gemm_8192_f16" and not nn \
+            and args.variant == "pipelined" and not args.out_f32 and not args.bias:
+        others = {}
+        if scrub is None:
+            scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+        for name, variant in OTHER_CONFIGS:
+            others[name + ("" if variant == "pipelined" else ":" + variant)] = measure_config(
+                sg, torch, dev, stream, gemm_inputs.WORKLOADS[name], variant, args.stages,
+                args.other_steps, 3, peaks, peak_src, scrub)
+
     long_region = elapsed_ms > 1000.0
     peak_key = "bf16_tflops_sustained" if long_region else "bf16_tflops"
     peak = float(peaks.get(peak_key, FALLBACK_TFLOPS))
@@ -738,6 +838,7 @@ def main():
             "sustained": sustained,
             "step_ms_dist": dist_ms,
             "cublas_context": cublas,
+            "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     plan.close()

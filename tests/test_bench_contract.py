@@ -143,3 +143,24 @@ def test_cpu_baseline_sample_reaches_both_ends_and_checks_parity():
     bad[rows - 1, 7] = float(bad[rows - 1, 7]) + 0.5
     st = bench.parity_of_rows(bad, ref, "f16", False)
     assert not st["ok"] and st["bad"] == 1
+
+
+@pytest.mark.gpu
+def test_gpu_bench_headline_line_carries_the_other_configurations():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = _run(["--steps", "3", "--warmup", "3", "--other-steps", "2", "--cpu-seconds", "1",
+              "--e2e-steps", "1", "--dist-reps", "0", "--sustained-seconds", "0.1"], timeout=900)
+    assert d["config"]["workload"] == "gemm_8192_f16" and d["parity"]["ok"]
+    o = d["other_configs"]
+    assert set(o) == {"gemm_256_f16", "gemm_4096_f16", "gemm_8192_f16:single_buffer",
+                      "gelu_3072x16384x4096_bf16", "ragged_4095x4097x8191_f16",
+                      "skinny_64x8192x8192_f16"}
+    for name, r in o.items():
+        assert r["value"] > 0 and r["ms_per_step"] > 0 and r["steps"] == 2, name
+        assert r["roofline"]["bound"] in ("tensor", "hbm") and r["roofline"]["frac"] > 0, name
+    assert o["skinny_64x8192x8192_f16"]["roofline"]["bound"] == "hbm"
+    assert o["ragged_4095x4097x8191_f16"]["kernels_per_step"] == 2
+    assert o["gemm_8192_f16:single_buffer"]["stages"] == 1
+    assert "cublas_context" in o["gemm_4096_f16"] and "cublas_context" not in o[
+        "gelu_3072x16384x4096_bf16"]
