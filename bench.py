@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--cta-group", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--k-serpentine", type=int, default=0, choices=[-1, 0, 1],
+                    help="K order of successive waves: 0 auto, 1 alternate, -1 always ascending")
     ap.add_argument("--tail-split", type=int, default=0,
                     help="K-splitting of the last partial wave: 0 auto, -1 off, k >= 2 forced")
     ap.add_argument("--layout", default="nt", choices=["nt", "nn"],
@@ -539,7 +541,7 @@ def main():
         args.stages = 1
     nn = args.layout == "nn"
     tuning = dict(tile_n=args.tile_n, raster_group=args.raster_group, cta_group=args.cta_group,
-                  tail_split=args.tail_split, b_kn=1 if nn else 0,
+                  tail_split=args.tail_split, k_serpentine=args.k_serpentine, b_kn=1 if nn else 0,
                   out_f32=1 if args.out_f32 else 0)
     A_cpu, B_cpu = gemm_inputs.make(w)
     if nn:  # the same draw, stored (K, N)
@@ -819,6 +821,7 @@ def main():
                 "stages": info["stages"], "tile": "%dx%dx%d" % (info["tile_m"], info["tile_n"],
                                                                info["tile_k"]),
                 "grid": info["grid"], "raster_group": info["raster_group"],
+                "k_serpentine": info["k_serpentine"],
                 "cta_group": info["cta_group"], "k_slices_per_slot": info["k_sub"],
                 "tail_splits": info["tail_splits"],
                 "tail_tiles": info["tail_tiles"],

@@ -488,13 +488,17 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
     if (want_bn != 0 && bn != want_bn) continue;
     if (want_cg != 0 && cg != want_cg) continue;
     // Eight epilogue warps where the epilogue is not hidden behind the main
-    // loop: short K, or a single row of tiles (8192 x 8192 x 512: 59.7 ->
-    // 55.3 us; 16896 x 512 x 640 13.3 -> 13.0 us).  Elsewhere four: a second
-    // epilogue warp on the MMA issuer's sub-partition cost 0.9 % of the
-    // cycles at 8192^3.
+    // loop: short K, a single row of tiles (8192 x 8192 x 512: 59.7 ->
+    // 55.3 us; 16896 x 512 x 640 13.3 -> 13.0 us), or a C whose rows are not
+    // 16-byte multiples, which is stored row by row instead of by the copy
+    // engine (4095 x 4097 x 8191: 241.1 -> 235.4 us).  Elsewhere four: a
+    // second epilogue warp on the MMA issuer's sub-partition cost 0.9 % of
+    // the cycles at 8192^3.
+    const bool rowwise_c = (N * ((tuning && tuning->out_f32) ? 4 : 2)) % 16 != 0;
     const int groups =
         (tuning && tuning->epi_groups) ? tuning->epi_groups
-                                       : ((cdiv(K, kBK) <= 16 || cdiv(std::max<int64_t>(M, 1), kBM * cg) == 1)
+                                       : ((cdiv(K, kBK) <= 16 || cdiv(std::max<int64_t>(M, 1), kBM * cg) == 1 ||
+                                           rowwise_c)
                                               ? 2
                                               : 1);
     int bufs = 2;

@@ -104,6 +104,16 @@ def test_short_k_gets_no_stream_k_and_eight_epilogue_warps():
     assert describe(8192, 8192, 1024 + 64, stages=6)["epi_groups"] == 1   # 17 slices
 
 
+def test_row_wise_c_stores_get_eight_epilogue_warps():
+    # A C whose rows are not 16-byte multiples is stored row by row (no bulk
+    # tensor store), which exposes the epilogue: eight warps.
+    assert describe(4095, 4097, 8191, stages=6)["epi_groups"] == 2
+    assert describe(4096, 4100, 8192, stages=6)["epi_groups"] == 2      # 8200 B rows
+    assert describe(4096, 4100, 8192, stages=6, out_f32=1)["epi_groups"] == 1  # 16400 B rows
+    assert describe(4096, 4104, 8192, stages=6)["epi_groups"] == 1      # 8208 B rows
+    assert describe(4095, 4097, 8191, stages=6, epi_groups=1)["epi_groups"] == 1
+
+
 def test_ring_is_capped_at_the_slices_of_short_k():
     assert describe(1024, 1024, 256, stages=6)["stages"] == 4
     assert describe(1024, 1024, 64 * 20, stages=6)["stages"] == 6
