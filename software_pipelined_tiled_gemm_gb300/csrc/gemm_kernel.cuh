@@ -472,10 +472,13 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
   ptx::tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   // Programmatic dependent launch: the set-up above touched no global memory
-  // and may overlap the previous kernel's tail; everything below (operand
-  // loads, C stores, workspace and status words) waits for it to finish.
+  // and may overlap the previous kernel's tail.  Each role waits for that
+  // kernel to finish right before its own first global-memory access: the
+  // producer before its first copy (so the work of finding its first unit
+  // overlaps the previous kernel too), the epilogue warps before anything
+  // else.  The MMA issuer reads only shared and tensor memory and does not
+  // wait.
   ptx::pdl_launch_dependents();
-  ptx::pdl_wait_prior_grid();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -486,6 +489,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
       // B read once (a single row of tiles): evict its lines from L2 first.
       const uint64_t pol_b = kStream ? ptx::l2_policy_evict_first() : 0;
       bool ok = true;
+      bool waited = false;  // on the previous kernel in the stream
       UnitIter it(walker, walkers, p);
       Unit x;
       while (ok && it.next(p, x)) {
@@ -540,6 +544,10 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
               ok = false;
               break;
             }
+          }
+          if (!waited) {
+            ptx::pdl_wait_prior_grid();
+            waited = true;
           }
           // Test hook: the first slice of CTA 0 is announced but never copied.
           const bool skip = p.inject_fault == 1 && blockIdx.x == 0 && x.seq == 0 && i == 0;
@@ -674,6 +682,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
     // Warp 2 + e: TMEM lane quarter q (rows q*32 .. q*32+31 of the CTA's
     // accumulator) and column group g = e / 4 of every unit.  Stream-K
     // partials, flags and fix-up barriers are per warp e.
+    ptx::pdl_wait_prior_grid();  // bias, workspace, flags and C are global
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int ew = warp - 2;      // epilogue warp index: staging, partials, flags
     const int g = ew / 4;         // column group
