@@ -58,6 +58,7 @@
 
 #include <cstdint>
 
+#include "byte_shift.cuh"
 #include "epilogue_math.cuh"
 #include "kernel_params.h"
 #include "ptx.cuh"
@@ -268,8 +269,12 @@ __device__ __forceinline__ void apply_epilogue32(uint32_t (&r)[32]) {
 // staging buffer in the layout of a 128-byte-swizzled TMA box (16-byte chunk
 // j of row r at j ^ (r % 8): bank-conflict free), then out with one TMA store
 // (double-buffered staging), or -- when C's pitch or address is not 16-byte
-// aligned -- row by row, each store instruction covering one contiguous row
-// segment.
+// aligned -- by the warp's own stores.  A whole block of 16-bit elements
+// goes four rows per step: eight lanes per row, lane j writing the row's
+// 16-byte-aligned chunk j (realigned from two staging chunks), and one
+// 2-byte store per lane for the row's unaligned head and tail, which
+// together always hold 8 elements.  A block cut by the edge of C goes row by
+// row, element by element.
 __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params& p,
                                            const CUtensorMap& tmC, uint8_t* my_stage, int& buf,
                                            int lane, int row0, int col0, int esize) {
@@ -308,6 +313,37 @@ __device__ __forceinline__ void store_rows(const uint32_t (&w)[32], const Params
     const int per_row = 128 / esize;                       // elements in the block's row
     const int ncols = min(per_row, p.N - col0);
     const int nrows = min(32, p.M - row0);
+    if (esize == 2 && ncols == 64 && nrows == 32) {
+      const uint32_t j = static_cast<uint32_t>(lane) & 7u;  // the 16-byte chunk this lane writes
+#pragma unroll 1
+      for (int r4 = 0; r4 < 32; r4 += 4) {
+        const uint32_t r = static_cast<uint32_t>(r4 + (lane >> 3));
+        uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) + (static_cast<int64_t>(row0 + r) * p.ldc + col0) * 2;
+        const uint32_t a = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(crow) & 15u);  // even
+        const uint8_t* srow = sb + r * 128u;
+        const uint32_t sw = r & 7u;                          // the row's chunk swizzle
+        if (a == 0) {
+          // Aligned row: chunk j is staging chunk j.
+          *reinterpret_cast<uint4*>(crow + 16u * j) = *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4));
+        } else {
+          // Aligned chunk j (1..7) holds row bytes [16j - a, 16j - a + 16):
+          // the end of staging chunk j - 1 and the start of chunk j.
+          if (j != 0) {
+            const uint4 lo = *reinterpret_cast<const uint4*>(srow + (((j - 1u) ^ sw) << 4));
+            const uint4 hi = *reinterpret_cast<const uint4*>(srow + ((j ^ sw) << 4));
+            *reinterpret_cast<uint4*>(crow - a + 16u * j) = shift_window(lo, hi, 16u - a);
+          }
+          // Head (row elements 0 .. h-1, h = (16 - a) / 2) and tail (the last
+          // a / 2 elements): 8 elements, one per lane of the row.
+          const uint32_t h = (16u - a) >> 1;
+          const uint32_t e = j < h ? j : 64u - 8u + j;       // row element of this lane
+          const uint32_t byte = 2u * e;
+          *reinterpret_cast<uint16_t*>(crow + byte) =
+              *reinterpret_cast<const uint16_t*>(srow + ((((byte >> 4) ^ sw)) << 4) + (byte & 15u));
+        }
+      }
+      return;
+    }
 #pragma unroll 1
     for (int r = 0; r < nrows; ++r) {
       uint8_t* crow = reinterpret_cast<uint8_t*>(p.C) +

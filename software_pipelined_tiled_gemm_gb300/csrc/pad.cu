@@ -13,24 +13,10 @@
 
 #include <cstdint>
 
+#include "byte_shift.cuh"
 #include "launch.h"
 
 namespace spgemm {
-
-// Bytes [off, off + 16) of the 32-byte little-endian value (lo, hi), off even.
-__device__ __forceinline__ uint4 shift_window(const uint4& lo, const uint4& hi, uint32_t off) {
-  const uint32_t q = off >> 2;          // whole 32-bit words to skip (0..3)
-  const uint32_t sh = (off & 3u) * 8u;  // then 0 or 16 more bits
-  uint32_t a0, a1, a2, a3, a4;
-  switch (q) {
-    case 0: a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x; break;
-    case 1: a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y; break;
-    case 2: a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z; break;
-    default: a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w; break;
-  }
-  return make_uint4(__funnelshift_r(a0, a1, sh), __funnelshift_r(a1, a2, sh),
-                    __funnelshift_r(a2, a3, sh), __funnelshift_r(a3, a4, sh));
-}
 
 __global__ void __launch_bounds__(256) pad_operands_kernel(const uint16_t* __restrict__ A, int64_t M,
                                                            uint16_t* __restrict__ Ap,
