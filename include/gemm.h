@@ -171,6 +171,10 @@ typedef struct {
                                   of a cluster, whose partial sum moves through
                                   distributed shared memory */
   int epi_groups;              /* epilogue column groups: 1 (four warps) or 2 (eight) */
+  int stream_k_first;          /* 1: each CTA takes its stream-K share before its whole tiles
+                                  (chosen when stream-K is on and the serpentine K order off),
+                                  so the fix-ups of shared tiles overlap later tiles; 0: the
+                                  stream-K share comes last */
 } gemm_plan_info_t;
 
 /* Create a plan for C = epi(A . B^T) of the given sizes on `device`.

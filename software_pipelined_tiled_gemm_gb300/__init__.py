@@ -90,7 +90,8 @@ class GemmPlanInfo(ctypes.Structure):
                 ("stream_k", ctypes.c_int), ("out_f32", ctypes.c_int), ("b_kn", ctypes.c_int),
                 ("k_sub", ctypes.c_int), ("host_panels", ctypes.c_int),
                 ("k_serpentine", ctypes.c_int), ("l2_prefetch_first", ctypes.c_int),
-                ("sk_cluster", ctypes.c_int), ("epi_groups", ctypes.c_int)]
+                ("sk_cluster", ctypes.c_int), ("epi_groups", ctypes.c_int),
+                ("stream_k_first", ctypes.c_int)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -129,6 +129,7 @@ struct gemm_plan {
   int k_serpentine = 0;          // odd waves walk K downwards
   int l2_prefetch_first = 0;     // prefetch the first ring's slices before the PDL wait
   int sk_cluster = 0;            // K halves exchanged within 2-CTA clusters
+  int sk_first = 0;              // stream-K share before the whole tiles
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -695,6 +696,12 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
   // 26.2 -> 25.6 us back to back).  L2-resident operands skip it: the
   // prefetches would only queue ahead of the ring's copies (16896 x 512 x
   // 640: 13.0 -> 13.9 us).
+  // Stream-K share first, whole tiles after: the owners' fix-ups then
+  // overlap their next tiles instead of ending the launch (GELU layer
+  // 3072 x 16384 x 4096 -3.3 %, 4096^3 -1.2 %).  Not with the serpentine K
+  // order, whose alternating waves it disturbs (K = 8192 shapes 2-5 %
+  // slower), nor for the cluster split, which has no whole tiles.
+  p->sk_first = (p->sk_tiles > 0 && !p->sk_cluster && !p->k_serpentine) ? 1 : 0;
   p->l2_prefetch_first = static_cast<double>(M + N) * static_cast<double>(K) * 2.0 >
                                  0.75 * static_cast<double>(dev.l2_bytes)
                              ? 1
@@ -1002,6 +1009,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.k_serpentine = plan->k_serpentine;
   prm.l2_prefetch_first = plan->l2_prefetch_first;
   prm.sk_cluster = plan->sk_cluster;
+  prm.sk_first = plan->sk_first;
   prm.inject_fault = plan->debug_fault;
   prm.prefetch_kb = plan->prefetch_kb;
   prm.a_box_rows = static_cast<int>(a_box_rows);
@@ -1238,6 +1246,7 @@ void fill_info(const gemm_plan* plan, gemm_plan_info_t* info) {
   info->b_kn = plan->b_kn;
   info->k_sub = plan->k_sub;
   info->host_panels = plan->num_panels >= 2 ? plan->num_panels : 0;
+  info->stream_k_first = plan->sk_first;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
 }
 

@@ -163,12 +163,15 @@ struct Unit {
   int k0, k1;  // K slices [k0, k1) of this piece
   int role;    // kWhole, kContrib (partial sum for another walker), kOwner (adds it, stores)
   int seq;     // running count of this walker's units
+  int wave;    // wave of whole tiles (walker's n-th whole tile), 0 for stream-K pieces
+  int skt;     // stream-K tile index of a stream-K piece, -1 otherwise
 };
 constexpr int kWhole = 0, kContrib = 1, kOwner = 2;
 
-// Enumerates a walker's units: first its whole tiles (and narrow tail
-// tiles), walker, walker + walkers, ...; then, with stream-K, its contiguous
-// share [begin, end) of the remaining sk_tiles * k_blocks K iterations.
+// Enumerates a walker's units: its whole tiles (and narrow tail tiles),
+// walker, walker + walkers, ...; and, with stream-K, its contiguous share
+// [begin, end) of the sk_tiles * k_blocks K iterations of the stream-K
+// tiles -- after the whole tiles, or before them with Params::sk_first.
 struct UnitIter {
   int u;
   int walkers;
@@ -182,9 +185,12 @@ struct UnitIter {
     }
   }
   __device__ bool next(const Params& p, Unit& x) {
+    if (p.sk_first && sk_it < sk_end) return next_sk(p, x);
     if (u < p.num_units) {
+      x.wave = u / walkers;
+      x.skt = -1;
       if (u < p.dp_tiles) {
-        x.tile = u;
+        x.tile = p.sk_first ? p.sk_tiles + u : u;
         x.sub = -1;
       } else {
         const int v = u - p.dp_tiles;
@@ -198,19 +204,23 @@ struct UnitIter {
       u += walkers;
       return true;
     }
-    if (sk_it < sk_end) {
-      const int64_t tl = sk_it / p.k_blocks;
-      x.tile = p.dp_tiles + static_cast<int>(tl);
-      x.sub = -1;
-      x.k0 = static_cast<int>(sk_it - tl * p.k_blocks);
-      const int64_t left = sk_end - sk_it;
-      x.k1 = static_cast<int>(x.k0 + left < p.k_blocks ? x.k0 + left : p.k_blocks);
-      x.role = (x.k0 == 0 && x.k1 == p.k_blocks) ? kWhole : (x.k0 > 0 ? kContrib : kOwner);
-      x.seq = seq++;
-      sk_it += x.k1 - x.k0;
-      return true;
-    }
+    if (sk_it < sk_end) return next_sk(p, x);
     return false;
+  }
+  // The next piece of this walker's stream-K share.
+  __device__ bool next_sk(const Params& p, Unit& x) {
+    const int64_t tl = sk_it / p.k_blocks;
+    x.skt = static_cast<int>(tl);
+    x.wave = 0;
+    x.tile = p.sk_first ? static_cast<int>(tl) : p.dp_tiles + static_cast<int>(tl);
+    x.sub = -1;
+    x.k0 = static_cast<int>(sk_it - tl * p.k_blocks);
+    const int64_t left = sk_end - sk_it;
+    x.k1 = static_cast<int>(x.k0 + left < p.k_blocks ? x.k0 + left : p.k_blocks);
+    x.role = (x.k0 == 0 && x.k1 == p.k_blocks) ? kWhole : (x.k0 > 0 ? kContrib : kOwner);
+    x.seq = seq++;
+    sk_it += x.k1 - x.k0;
+    return true;
   }
 };
 
@@ -549,7 +559,8 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             CG * kSub;
         const int nk = x.k1 - x.k0;
         const int kr = k_start(x, walker, walkers, p);
-        const bool down = p.k_serpentine && (x.seq & 1) && x.role == kWhole;
+        const bool down =
+            p.k_serpentine && ((p.sk_first ? x.wave : x.seq) & 1) && x.role == kWhole;
         for (int i = 0, kf = x.k0 + kr; i < nk; ++i, kf = (kf + 1 == x.k1) ? x.k0 : kf + 1) {
           const int kb = down ? x.k1 - 1 - i : kf;  // K slot this iteration copies
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, p, kDetailProducerEmpty)) {
@@ -763,7 +774,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
       // Stream-K: this warp's fp32 partial of a shared tile, laid out
       // [column - c_lo][lane] (one coalesced 128-byte line per column).
       const uint32_t flag_idx =
-          (static_cast<uint32_t>(x.tile - p.dp_tiles) * CG + rank) * (4u * epi_groups) + ew;
+          (static_cast<uint32_t>(x.skt) * CG + rank) * (4u * epi_groups) + ew;
       float* partial = (kSplit && x.role != kWhole)
                            ? p.sk_ws + static_cast<size_t>(flag_idx) * (warp_partial / 4u)
                            : nullptr;
@@ -850,6 +861,16 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
           fix_phase ^= 1u;
           have_partial = true;
         }
+      } else if (kSplit && x.role == kOwner && has_cols && p.sk_first) {
+        // The other walker's partial was its first piece, long published:
+        // wait for its flag (usually already raised) and read the partial
+        // from L2 in the adds below; the ring is busy with the next tile.
+        int ok = 1;
+        if (lane == 0) ok = wait_flag(p.sk_flags + flag_idx, p, kDetailSkFlag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        (void)ld_acquire_gpu(p.sk_flags + flag_idx);  // every lane acquires the partial
+        have_partial = true;
       } else if (kSplit && x.role == kOwner && has_cols) {
         // The other walker's partial (K slices [k1, k_blocks)) was written at
         // the start of its range.  This is the last unit of this walker, so
@@ -884,7 +905,16 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
           ptx::tmem_ld_32x32b_x32(t_row + cc, r0);
           ptx::tmem_ld_32x32b_x32(t_row + cc + 32, r1);
           ptx::tmem_wait_ld();
-          if (kSplit && have_partial) {
+          if (kSplit && have_partial && p.sk_first && !p.sk_cluster) {
+            // own slices first, then the partial (from L2): a fixed order on every run
+            const int cb = cc - c_lo;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              r0[j] = __float_as_uint(__uint_as_float(r0[j]) + __ldcg(partial + (cb + j) * 32 + lane));
+              r1[j] = __float_as_uint(__uint_as_float(r1[j]) +
+                                      __ldcg(partial + (cb + 32 + j) * 32 + lane));
+            }
+          } else if (kSplit && have_partial) {
             // own slices first, then the partial: a fixed order on every run
             const int cb = cc - c_lo;
 #pragma unroll
@@ -922,6 +952,10 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             store_rows(pk, p, tmC, my_stage, buf, lane, row0, col0 + 32 * h, p.out_f32 ? 4 : 2);
           }
         }
+      }
+      if (kSplit && p.sk_first && !p.sk_cluster && x.role == kOwner && has_cols) {
+        __syncwarp();                               // every lane has read the partial
+        if (lane == 0) p.sk_flags[flag_idx] = 0;    // ready for the next launch
       }
       // This warp's TMEM reads of accumulator `acc` are complete (wait::ld).
       ptx::tc_fence_before_sync();

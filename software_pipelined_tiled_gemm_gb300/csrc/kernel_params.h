@@ -100,6 +100,14 @@ struct Params {
   int sk_tiles;
   float* sk_ws;
   int* sk_flags;
+  // 1: each walker takes its stream-K share first and its whole tiles after
+  // (the stream-K tiles are then tiles [0, sk_tiles) and the whole ones
+  // follow).  A contributor's piece is the first of its share, so its
+  // partial is published early; the owner's fix-up reads it from L2 and
+  // overlaps the walker's next tile instead of ending the launch.  0: whole
+  // tiles first, stream-K tiles [dp_tiles, num_tiles) last, the owner staging
+  // the partial in its then idle ring.
+  int sk_first;
   int sk_slots;          // epilogue-warp partials (and flags) sk_ws / sk_flags hold
   // 1: each unit starts its K loop at a different slice (wrapping around),
   // so CTAs that share the same A rows do not all read the same A slice at

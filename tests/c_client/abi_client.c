@@ -85,6 +85,7 @@ static int layout(void) {
   OFF(gemm_plan_info_t, "info", l2_prefetch_first);
   OFF(gemm_plan_info_t, "info", sk_cluster);
   OFF(gemm_plan_info_t, "info", epi_groups);
+  OFF(gemm_plan_info_t, "info", stream_k_first);
 
   printf("sizeof device %lu\n", (unsigned long)sizeof(gemm_device_desc_t));
   OFF(gemm_device_desc_t, "device", sm_count);

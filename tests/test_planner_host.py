@@ -242,3 +242,19 @@ def test_device_query_without_a_gpu_fails_cleanly():
         pytest.skip("a GPU is present")
     st, _ = sg.gemm_device_query(0)
     assert st in (sg.GEMM_ERR_CUDA, sg.GEMM_ERR_INVALID_ARG, sg.GEMM_ERR_UNSUPPORTED)
+
+
+def test_stream_k_share_first_unless_serpentine():
+    # Stream-K plans take their stream-K share before their whole tiles,
+    # except with the serpentine K order (whose alternating waves the
+    # reordering disturbs) and the cluster split (no whole tiles).
+    d = describe(4096, 4096, 4096, stages=6)
+    assert d["stream_k"] == 1 and d["k_serpentine"] == 0 and d["stream_k_first"] == 1
+    assert describe(3072, 16384, 4096, "bf16", epilogue="gelu", stages=6)["stream_k_first"] == 1
+    d = describe(8192, 8192, 8192, stages=6)
+    assert d["stream_k"] == 1 and d["k_serpentine"] == 1 and d["stream_k_first"] == 0
+    assert describe(4096, 4096, 4096, stages=6, k_serpentine=1)["stream_k_first"] == 0
+    d = describe(128, 8192, 2048, stages=6)
+    assert d["sk_cluster"] == 1 and d["stream_k_first"] == 0
+    assert describe(2048, 2048, 2048, stages=6)["stream_k"] == 0
+    assert describe(2048, 2048, 2048, stages=6)["stream_k_first"] == 0
