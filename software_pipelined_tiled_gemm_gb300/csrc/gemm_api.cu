@@ -456,6 +456,11 @@ gemm_status_t device_props(int device, gemm_device_desc_t* desc) {
 // corresponding fields of *p.  Host arithmetic only, except what
 // `pair_clusters` does; allocates nothing (on failure *p is left to the
 // caller to discard).
+// Rows of A one K slice of the ring holds: all kBM rows of the CTA's tile,
+// or 64 for single-CTA tiles when M <= 64 (then a single row of tiles, run by
+// the evict-first-B instances, which size their A slices from the box).
+int ring_a_rows(int cta_group, int64_t M) { return (cta_group == 1 && M <= 64) ? 64 : kBM; }
+
 gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
                           PairClustersFn pair_clusters, void* ctx, int64_t M, int64_t N,
                           int64_t K, gemm_dtype_t dtype, gemm_epilogue_t epi, int stages,
@@ -503,10 +508,11 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
                                               ? 2
                                               : 1);
     int bufs = 2;
-    size_t need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
+    const int a_rows = ring_a_rows(cg, M);
+    size_t need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups, a_rows);
     if (need > static_cast<size_t>(dev.smem_optin)) {
       bufs = 1;
-      need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups);
+      need = kernel_smem_bytes(bn, ring_stages, bufs, cg, groups, a_rows);
     }
     if (need > static_cast<size_t>(dev.smem_optin)) continue;
     const int64_t tiles =
@@ -536,7 +542,8 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
     if (cg == 1 && variant == GEMM_PIPELINED && want_split != -1 &&
         2 * tiles <= dev.sm_count && 10 * 2 * tiles >= 8 * dev.sm_count &&
         cdiv(K, kBK) >= 16 && cdiv(K, kBK) % 2 == 0 &&
-        static_cast<int64_t>(ring_stages) * (kStageA + static_cast<int64_t>(bn) * kBK * 2) >=
+        static_cast<int64_t>(ring_stages) *
+                (static_cast<int64_t>(ring_a_rows(cg, M)) * kBK * 2 + static_cast<int64_t>(bn) * kBK * 2) >=
             static_cast<int64_t>(epi_cta_partial_bytes(bn, groups)))
       break;
   }
@@ -610,8 +617,9 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
   p->dp_tiles = p->num_tiles;
   p->tail_splits = 1;
   p->sk_tiles = 0;
+  const int64_t slice_a = static_cast<int64_t>(ring_a_rows(chosen_cg, M)) * kBK * 2;
   const int64_t ring_all = static_cast<int64_t>(ring_stages) *
-                           (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
+                           (slice_a + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
   const bool ring_holds_partial =
       ring_all >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
   if (variant == GEMM_PIPELINED && want_split == 0 && chosen_cg == 1 && p->num_tiles > 0 &&
@@ -629,7 +637,7 @@ gemm_status_t plan_layout(gemm_plan* p, const gemm_device_desc_t& dev,
   } else if (variant == GEMM_PIPELINED && want_split != -1 && p->num_tiles > 0) {
     const int64_t rem = p->num_tiles % walkers;
     const int64_t ring = static_cast<int64_t>(ring_stages) *
-                         (kStageA + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
+                         (slice_a + static_cast<int64_t>(p->bn / chosen_cg) * kBK * 2);
     const bool sk_fits = ring >= static_cast<int64_t>(epi_cta_partial_bytes(p->bn, p->epi_groups));
     // Automatic stream-K needs long tiles: exchanging one partial costs about
     // as much as a few K slices, so with short K it loses more than the idle
@@ -926,7 +934,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
       (static_cast<size_t>(N) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
 
   // M <= 64 (single CTA tiles): copy only 64 rows of A per slice.
-  const uint32_t a_box_rows = (plan->cg == 1 && M <= 64) ? 64u : static_cast<uint32_t>(kBM);
+  const uint32_t a_box_rows = static_cast<uint32_t>(ring_a_rows(plan->cg, M));
   if (plan->mapA_ptr != effA || plan->mapK != Keff) {
     st = encode_2d(&plan->tmA, plan->dtype, effA, Keff, M, Keff, kBK, a_box_rows,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);

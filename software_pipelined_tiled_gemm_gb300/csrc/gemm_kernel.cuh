@@ -403,8 +403,14 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
   constexpr int kBRows = BN / CG;                    // B rows this CTA loads
   constexpr uint32_t kStageB = kBRows * kBK * 2;     // B bytes of one K slice
   constexpr uint32_t kBBlocks = kBRows / 64;           // 64-column blocks of a K x N B slice
-  constexpr uint32_t kSlotA = kStageA * kSub;        // A part of a slot
-  constexpr uint32_t kStage = kSlotA + kStageB * kSub;  // bytes per slot, this CTA
+  // A bytes of one K slice in the ring: the whole 128-row box, except that a
+  // single row of single-CTA tiles with M <= 64 copies (and keeps) only 64
+  // rows -- the MMA's rows 64-127 then read the next bytes of the slot, and
+  // feed only output rows >= M, which are never stored.  The freed space
+  // holds more slices (M = 64: 8 slices of 128-column B instead of 6).
+  const uint32_t kSliceA = kStream ? static_cast<uint32_t>(p.a_box_rows) * (kBK * 2u) : kStageA;
+  const uint32_t kSlotA = kSliceA * kSub;             // A part of a slot
+  const uint32_t kStage = kSlotA + kStageB * kSub;    // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
   static_assert(kEpiG == 1 || kEpiG == 2, "one or two epilogue column groups");
   constexpr int epi_groups = kEpiG;  // epilogue column groups (4 x kEpiG epilogue warps)
@@ -608,7 +614,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             for (int sub = 0; sub < kSub; ++sub) {
               if (skip) break;
               const int kx = (kb * kSub + sub) * kBK;  // first K element of this slice
-              const uint32_t da = sa + sub * kStageA, db = sa + kSlotA + sub * kStageB;
+              const uint32_t da = sa + sub * kSliceA, db = sa + kSlotA + sub * kStageB;
               ptx::tma_load_2d_pair(da, &tmA, kx, a_row, fb);
               if constexpr (!kKN)
                 ptx::tma_load_2d_pair(db, tmb, kx, b_row, fb);
@@ -621,7 +627,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             for (int sub = 0; sub < kSub; ++sub) {
               if (skip) break;
               const int kx = (kb * kSub + sub) * kBK;
-              const uint32_t da = sa + sub * kStageA, db = sa + kSlotA + sub * kStageB;
+              const uint32_t da = sa + sub * kSliceA, db = sa + kSlotA + sub * kStageB;
               ptx::tma_load_2d(da, &tmA, kx, a_row, full_bar(stage));
               if constexpr (!kKN && !kStream)
                 ptx::tma_load_2d(db, tmb, kx, b_row, full_bar(stage));
@@ -691,11 +697,11 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
           for (int k = 0; k < kSub * (kBK / kUmmaK); ++k) {
             // Within a slice, +32 bytes along K inside the 128-byte swizzled
             // row = +2 in the descriptor's address field (16-byte units); the
-            // second slice of a slot starts kStageA (A) / kStageB (B) later.
+            // second slice of a slot starts kSliceA (A) / kStageB (B) later.
             // K x N B: the slices' row groups follow each other, +2 groups
             // per step throughout.
             const uint32_t sub = static_cast<uint32_t>(k) / 4u, kk = static_cast<uint32_t>(k) % 4u;
-            const uint64_t ad = a_desc + sub * (kStageA / 16u) + 2u * kk;
+            const uint64_t ad = a_desc + sub * (kSliceA / 16u) + 2u * kk;
             const uint64_t bd = kKN ? b_desc + b_step * static_cast<uint32_t>(k)
                                     : b_desc + sub * (kStageB / 16u) + 2u * kk;
             ptx::mma_f16_ss<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);

@@ -177,10 +177,13 @@ __host__ __device__ constexpr size_t epi_cta_partial_bytes(int bn, int groups) {
 // Shared memory a CTA needs for a given tile width / ring depth / staging
 // (store_bufs buffers for each of the epi_groups x 4 active epilogue warps);
 // with a CTA pair (cta_group 2) each CTA holds half of the tile's B rows.
+// Dynamic shared memory of a kernel launch: `stages` K slices of A (a_rows
+// rows: kBM, or 64 for a single row of single-CTA tiles with M <= 64) and B,
+// the epilogue staging buffers and the barriers.
 inline size_t kernel_smem_bytes(int bn, int stages, int store_bufs, int cta_group = 1,
-                                int epi_groups = 1) {
+                                int epi_groups = 1, int a_rows = kBM) {
   const size_t stage =
-      static_cast<size_t>(kStageA) + static_cast<size_t>(bn / cta_group) * kBK * 2;
+      static_cast<size_t>(a_rows) * kBK * 2 + static_cast<size_t>(bn / cta_group) * kBK * 2;
   return kAlignSlack + stage * static_cast<size_t>(stages) +
          static_cast<size_t>(4 * epi_groups) * store_bufs * kStoreBuf + kBarrierBytes;
 }

@@ -582,6 +582,22 @@ def test_hundred_runs_bit_identical():
     assert st["ok"], st
 
 
+@pytest.mark.parametrize("stages", [5, 6, 7, 8])
+@pytest.mark.parametrize("M,b_kn", [(1, 0), (33, 0), (64, 0), (64, 1)])
+def test_sixty_four_row_a_slices_every_ring_depth_bit_exact(M, b_kn, stages):
+    # M <= 64: the ring keeps 64-row A slices, so up to 8 slices of 128-wide
+    # B fit; odd depths run one slice per slot, even ones >= 6 two.  Tiles
+    # split into K halves (N = 4096) and not (N = 8192, tile_n 64).
+    for N, tuning in ((4096, {}), (8192, {"tile_n": 64})):
+        K = 2048
+        A, B = _int_inputs(M, N, K, "f16", seed=M * 5 + stages + N)
+        Bdev = B.t().contiguous() if b_kn else B
+        C, info, canary = gu.run_device(A, Bdev, "f16", stages=stages, b_kn=b_kn, **tuning)
+        assert canary and info["stages"] == stages, info
+        assert info["k_sub"] == (2 if stages % 2 == 0 and stages >= 6 else 1), info
+        _assert_bit_exact(A, B, "f16", C)
+
+
 @pytest.mark.parametrize("shape", [(64, 4096, 2048), (40, 2048, 1024), (128, 2048, 4096),
                                    (200, 1024, 2048), (64, 8192, 1100)])
 def test_few_tiles_split_k_in_two_bit_exact(shape):

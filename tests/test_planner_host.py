@@ -258,3 +258,15 @@ def test_stream_k_share_first_unless_serpentine():
     assert d["sk_cluster"] == 1 and d["stream_k_first"] == 0
     assert describe(2048, 2048, 2048, stages=6)["stream_k"] == 0
     assert describe(2048, 2048, 2048, stages=6)["stream_k_first"] == 0
+
+
+def test_sixty_four_row_a_slices_leave_room_for_deeper_rings():
+    # M <= 64 keeps 64-row A slices (8 KiB instead of 16), so the skinny
+    # 64 x 8192 x 8192 plan fits 8 slices of 128-wide B split in K halves;
+    # with M = 65 the full 128-row slices leave room for 6 only at that width.
+    d64 = describe(64, 8192, 8192, stages=8)
+    assert d64["tile_n"] == 128 and d64["sk_cluster"] == 1 and d64["smem_bytes"] <= 232448
+    # (at 8 slices the epilogue staging is single-buffered to make room)
+    assert describe(64, 8192, 8192, stages=6)["smem_bytes"] < d64["smem_bytes"]
+    assert describe(65, 8192, 8192, stages=8)["tile_n"] == 64
+    assert describe(65, 8192, 8192, stages=6)["tile_n"] == 128
