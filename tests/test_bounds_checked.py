@@ -97,6 +97,11 @@ _GPU_CHILD = """
         (300, 520, 1001, "f16", None, 4, "pipelined", {}),
         (512, 768, 1024, "f16", None, 6, "pipelined", {"cta_group": 2, "k_serpentine": 1,
                                                       "max_ctas": 4, "epi_groups": 2}),
+        # M <= 64: 64-row A slices, 8 slices in flight (K halves in clusters;
+        # whole K on 64-wide tiles; B stored K x N)
+        (64, 4096, 2048, "f16", None, 8, "pipelined", {}),
+        (33, 8192, 2048, "f16", None, 8, "pipelined", {"tile_n": 64}),
+        (64, 2048, 1024, "f16", None, 8, "pipelined", {"b_kn": 1}),
     ]
     results = []
     for i, (M, N, K, dt, epi, stages, variant, tuning) in enumerate(cases):
