@@ -408,9 +408,9 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
   // rows -- the MMA's rows 64-127 then read the next bytes of the slot, and
   // feed only output rows >= M, which are never stored.  The freed space
   // holds more slices (M = 64: 8 slices of 128-column B instead of 6).
-  const uint32_t kSliceA = kStream ? static_cast<uint32_t>(p.a_box_rows) * (kBK * 2u) : kStageA;
-  const uint32_t kSlotA = kSliceA * kSub;             // A part of a slot
-  const uint32_t kStage = kSlotA + kStageB * kSub;    // bytes per slot, this CTA
+  const uint32_t slice_a = kStream ? static_cast<uint32_t>(p.a_box_rows) * (kBK * 2u) : kStageA;
+  const uint32_t slot_a = slice_a * kSub;              // A part of a slot
+  const uint32_t slot_bytes = slot_a + kStageB * kSub;  // bytes per slot, this CTA
   constexpr int kTileM = kBM * CG;                   // output rows per tile
   static_assert(kEpiG == 1 || kEpiG == 2, "one or two epilogue column groups");
   constexpr int epi_groups = kEpiG;  // epilogue column groups (4 x kEpiG epilogue warps)
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
   const uint32_t sbase = ptx::smem_addr(smem);
 
   const int S = p.stages;
-  const uint32_t ring_bytes = static_cast<uint32_t>(S) * kStage;
+  const uint32_t ring_bytes = static_cast<uint32_t>(S) * slot_bytes;
   uint8_t* staging = smem + ring_bytes;
   const uint32_t staging_bytes = 4u * epi_groups * p.store_bufs * kStoreBuf;
   const uint32_t bar_base = sbase + ring_bytes + staging_bytes;
@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             if (pk >= x.k1) pk -= (x.k1 - x.k0);
             if (pk >= x.k0 && pk < x.k1) ptx::tma_prefetch_l2_2d(&tmBp, pk * kBK, b_row);
           }
-          const uint32_t sa = sbase + stage * kStage;
+          const uint32_t sa = sbase + stage * slot_bytes;
           // Copy coordinates: the K slot inside the unit's range, the first K
           // element 16-byte aligned (x of a tiled copy) and inside the K
           // extent, the rows inside the tile grid.  Test hook 2 makes this
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             for (int sub = 0; sub < kSub; ++sub) {
               if (skip) break;
               const int kx = (kb * kSub + sub) * kBK;  // first K element of this slice
-              const uint32_t da = sa + sub * kSliceA, db = sa + kSlotA + sub * kStageB;
+              const uint32_t da = sa + sub * slice_a, db = sa + slot_a + sub * kStageB;
               ptx::tma_load_2d_pair(da, &tmA, kx, a_row, fb);
               if constexpr (!kKN)
                 ptx::tma_load_2d_pair(db, tmb, kx, b_row, fb);
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             for (int sub = 0; sub < kSub; ++sub) {
               if (skip) break;
               const int kx = (kb * kSub + sub) * kBK;
-              const uint32_t da = sa + sub * kSliceA, db = sa + kSlotA + sub * kStageB;
+              const uint32_t da = sa + sub * slice_a, db = sa + slot_a + sub * kStageB;
               ptx::tma_load_2d(da, &tmA, kx, a_row, full_bar(stage));
               if constexpr (!kKN && !kStream)
                 ptx::tma_load_2d(db, tmb, kx, b_row, full_bar(stage));
@@ -684,24 +684,24 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
             break;
           }
           ptx::tc_fence_after_sync();
-          const uint32_t sa = sbase + stage * kStage;
+          const uint32_t sa = sbase + stage * slot_bytes;
           const uint64_t a_desc = ptx::smem_desc_k_sw128(sa);
           // K-major B: +32 B per 16-wide K step inside the swizzled row (+2 in
           // 16-byte units).  MN-major B (atoms [K group][column block], the
           // column blocks of one K group adjacent): +2 K groups per step.
           const uint64_t b_desc =
-              kKN ? ptx::smem_desc_mn_sw128(sa + kSlotA, 1024u, kBBlocks * 1024u)
-                  : ptx::smem_desc_k_sw128(sa + kSlotA);
+              kKN ? ptx::smem_desc_mn_sw128(sa + slot_a, 1024u, kBBlocks * 1024u)
+                  : ptx::smem_desc_k_sw128(sa + slot_a);
           constexpr uint32_t b_step = kKN ? 2u * kBBlocks * 1024u / 16u : 2u;
 #pragma unroll
           for (int k = 0; k < kSub * (kBK / kUmmaK); ++k) {
             // Within a slice, +32 bytes along K inside the 128-byte swizzled
             // row = +2 in the descriptor's address field (16-byte units); the
-            // second slice of a slot starts kSliceA (A) / kStageB (B) later.
+            // second slice of a slot starts slice_a (A) / kStageB (B) later.
             // K x N B: the slices' row groups follow each other, +2 groups
             // per step throughout.
             const uint32_t sub = static_cast<uint32_t>(k) / 4u, kk = static_cast<uint32_t>(k) % 4u;
-            const uint64_t ad = a_desc + sub * (kSliceA / 16u) + 2u * kk;
+            const uint64_t ad = a_desc + sub * (slice_a / 16u) + 2u * kk;
             const uint64_t bd = kKN ? b_desc + b_step * static_cast<uint32_t>(k)
                                     : b_desc + sub * (kStageB / 16u) + 2u * kk;
             ptx::mma_f16_ss<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
