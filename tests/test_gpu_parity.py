@@ -154,6 +154,19 @@ def test_edge_shapes(shape, dtype):
     assert info["tma_store"] == (0 if N % 8 else 1)
 
 
+@pytest.mark.parametrize("shape,dtype", [((70001, 24, 40), "f16"), ((5, 70001, 48), "f16"),
+                                         ((40000, 130, 8), "bf16"), ((3000, 3000, 3), "f16")])
+def test_many_tiles_along_one_dimension_bit_exact(shape, dtype):
+    # Hundreds of tiles along one dimension with the other two tiny: many
+    # raster groups (or one row of hundreds of tiles), single-slice K, ragged
+    # edges on every side.
+    M, N, K = shape
+    A, B = _int_inputs(M, N, K, dtype, seed=M + 3 * N + 7 * K)
+    C, info, canary = gu.run_device(A, B, dtype)
+    assert canary and info["num_tiles"] >= 128, info
+    _assert_bit_exact(A, B, dtype, C)
+
+
 @pytest.mark.parametrize("stages", [1, 2, 4])
 def test_gelu_bf16_small(stages):
     A, B = gemm_inputs.make("gelu_3072x16384x4096_bf16", M=192, N=640, K=512)
