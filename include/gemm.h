@@ -161,8 +161,9 @@ typedef struct {
   int b_kn;                    /* B is stored K x N */
   int k_sub;                   /* K slices of tile_k per ring slot: stages / k_sub
                                   slots of k_sub slices each (same shared memory) */
-  int host_panels;             /* row panels gemm_run_host pipelines its copies in
-                                  (0 before the first pipelined call) */
+  int host_panels;             /* blocks of C (row panels x column panels) gemm_run_host
+                                  pipelines its copies in (0 before the first pipelined
+                                  call) */
   int k_serpentine;            /* 1: successive waves alternate their K direction */
   int l2_prefetch_first;       /* 1: operands exceed 3/4 of L2, so each CTA prefetches its first
                                   ring's slices into L2 before waiting on the previous
@@ -232,14 +233,18 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
  * asynchronous copies; pageable memory works too.  The first call allocates
  * the device buffers.
  *
- * Problems with at least 32 MiB of copies and M >= 2048 run as 2-4 row
- * panels so that copies overlap the GEMM.  B comes in first, split over two
- * plan-owned copy streams.  The panels of A follow, alternating between
- * them.  Each panel's GEMM runs on `stream` as soon as its rows are in,
- * through a panel plan of its own.  Its rows of C go back on a third copy
- * stream while the next panel computes.  The copy streams wait for the work
- * already queued on `stream`, and the call returns after all of them
- * finish.  gemm_plan_check also reports the panel plans' device status. */
+ * Problems with at least 32 MiB of copies and at least 2 blocks run in
+ * blocks of C so that copies overlap the GEMM: 1-4 row panels of >= 1536 rows
+ * (whole tiles), and -- for B stored N x K with K % 8 == 0 -- 1-4 column
+ * panels of >= 1536 columns (multiples of 256; otherwise whole rows of C).
+ * The panels of A and of B (rows of B for a column panel, else all of B)
+ * come in on one plan-owned copy stream, alternating A0, B0, A1, B1, ..., and
+ * each block's GEMM runs on `stream` as soon as its two panels are in,
+ * through a block plan of its own.  The block of C goes back (a 2-D copy) on
+ * a second copy stream while the next blocks compute.  The copy streams wait
+ * for the work already queued on `stream`, and the call returns after all of
+ * them finish.  gemm_plan_check also reports the block plans' device
+ * status. */
 gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, void* hC,
                             int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                             gemm_epilogue_t epi, int stages, void* stream);

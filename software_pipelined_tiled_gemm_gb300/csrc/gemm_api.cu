@@ -92,9 +92,12 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 }  // namespace
 
 // gemm_run_host splits problems of at least kHostPanelMinBytes of copies into
-// up to kHostPanelsMax row panels of at least kHostPanelMinRows rows.
+// blocks of C: up to kHostPanelsMax row panels and as many column panels, each
+// at least kHostPanelMinRows rows / columns (smaller blocks run as GEMMs too
+// short to keep the SMs busy: 4096^3 took 0.526 ms in 16 blocks of 1024,
+// 0.487 ms in 4 of 2048).
 constexpr int kHostPanelsMax = 4;
-constexpr int64_t kHostPanelMinRows = 1024;
+constexpr int64_t kHostPanelMinRows = 1536;
 constexpr size_t kHostPanelMinBytes = 32u << 20;
 
 // Automatic stream-K also needs the last, partial wave to leave each walker
@@ -130,6 +133,9 @@ struct gemm_plan {
   int l2_prefetch_first = 0;     // prefetch the first ring's slices before the PDL wait
   int sk_cluster = 0;            // K halves exchanged within 2-CTA clusters
   int sk_first = 0;              // stream-K share before the whole tiles
+  // C's row pitch in elements when it differs from N: the block plans of
+  // gemm_run_host write a block of a wider C (0 = N).
+  int64_t ldc = 0;
 
   int* d_status = nullptr;       // [0] code, [1] detail
   int64_t dp_tiles = 0;          // tiles run whole
@@ -154,18 +160,22 @@ struct gemm_plan {
   void* hA = nullptr;
   void* hB = nullptr;
   void* hC = nullptr;
-  // gemm_run_host pipelining (see gemm_run_host): row panels of A and C, run
-  // by panel plans of their own; copies in on two streams, out on a third.
+  // gemm_run_host pipelining (see gemm_run_host): blocks of C, panel_rows x
+  // panel_cols (shorter at the ends), each run by a block plan of its own
+  // (blk[last row panel][last column panel]); copies in on one stream, in the
+  // order the blocks can start, and out on a second.
   gemm_tuning_t tuning{};
   bool has_tuning = false;
-  int64_t panel_rows = 0;          // 0: no row panels yet chosen
-  int num_panels = 0;
-  gemm_plan* panel_full = nullptr;  // plan for panel_rows rows
-  gemm_plan* panel_last = nullptr;  // plan for a shorter last panel, if any
-  cudaStream_t copy_in[2] = {nullptr, nullptr};
+  int64_t panel_rows = 0;          // 0: no blocks yet chosen
+  int64_t panel_cols = 0;
+  int num_panels = 0;              // row panels
+  int num_col_panels = 0;          // column panels
+  gemm_plan* blk[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
+  cudaStream_t copy_in = nullptr;
   cudaStream_t copy_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_b[2] = {nullptr, nullptr}, ev_done = nullptr;
-  cudaEvent_t ev_a[kHostPanelsMax] = {}, ev_c[kHostPanelsMax] = {};
+  cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_a[kHostPanelsMax] = {}, ev_b[kHostPanelsMax] = {};
+  cudaEvent_t ev_c[kHostPanelsMax * kHostPanelsMax] = {};
 
   int last_pads = 0;
   int last_tma_store = 0;
@@ -825,9 +835,11 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   const size_t esC = plan->out_f32 ? 4 : 2;   // bytes per element of C
   const size_t bytesA = static_cast<size_t>(M) * K * 2, bytesB = static_cast<size_t>(N) * K * 2;
   const size_t bytesC = static_cast<size_t>(M) * N * esC;
-  if (ranges_overlap(C, bytesC, A, bytesA) || ranges_overlap(C, bytesC, B, bytesB))
+  const int64_t ldc = plan->ldc ? plan->ldc : N;  // C's row pitch (elements)
+  const size_t extentC = (static_cast<size_t>(M - 1) * ldc + N) * esC;
+  if (ranges_overlap(C, extentC, A, bytesA) || ranges_overlap(C, extentC, B, bytesB))
     return fail(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
-  if (bias && ranges_overlap(C, bytesC, bias, static_cast<size_t>(N) * 2))
+  if (bias && ranges_overlap(C, extentC, bias, static_cast<size_t>(N) * 2))
     return fail(GEMM_ERR_INVALID_ARG, "C overlaps the bias");
   if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
         reinterpret_cast<uintptr_t>(bias)) & 1u) ||
@@ -931,7 +943,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   const int64_t Beff_rows = plan->b_kn ? (padB ? Bp_rows : K) : N;
 
   const bool tma_store =
-      (static_cast<size_t>(N) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
+      (static_cast<size_t>(ldc) * esC) % 16 == 0 && (reinterpret_cast<uintptr_t>(C) & 15u) == 0;
 
   // M <= 64 (single CTA tiles): copy only 64 rows of A per slice.
   const uint32_t a_box_rows = static_cast<uint32_t>(ring_a_rows(plan->cg, M));
@@ -970,8 +982,8 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   plan->mapK = Keff;
   if (tma_store && plan->mapC_ptr != C) {
     // One 128-byte row of 16-bit (64) or fp32 (32) elements per box row.
-    st = plan->out_f32 ? encode_2d_f32(&plan->tmC, C, N, M, N, 32, 32)
-                       : encode_2d(&plan->tmC, plan->dtype, C, N, M, N, kStoreCols, 32,
+    st = plan->out_f32 ? encode_2d_f32(&plan->tmC, C, N, M, ldc, 32, 32)
+                       : encode_2d(&plan->tmC, plan->dtype, C, N, M, ldc, kStoreCols, 32,
                                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
     if (st != GEMM_OK) return st;
     plan->mapC_ptr = C;
@@ -1003,7 +1015,7 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   prm.idesc = ptx::instr_desc_f16(kBM * plan->cg, plan->bn, plan->dtype == GEMM_BF16,
                                   plan->b_kn != 0);
   prm.C = C;
-  prm.ldc = N;
+  prm.ldc = ldc;
   prm.status = plan->d_status;
   prm.timeout_ns = plan->timeout_ns;
   prm.dp_tiles = static_cast<int>(plan->dp_tiles);
@@ -1041,44 +1053,58 @@ gemm_status_t gemm_run_bias(gemm_plan_t* plan, const void* A, const void* B, con
   return GEMM_OK;
 }
 
-// Row panels for gemm_run_host: plans of panel_rows rows (and a shorter last
-// panel), plus the copy streams and events, made on first use.
+// Blocks for gemm_run_host.  Row panels of A (whole tiles of rows); column
+// panels -- row panels of B -- only for N x K B and K a multiple of 8, so
+// that every block's A and B rows start 16-byte aligned inside the staged
+// operands (B stored K x N, or a K that needs padding, keeps whole rows of
+// C).  One plan per block shape, writing into the whole C (row pitch N).
 static gemm_status_t host_panels_setup(gemm_plan_t* plan) {
   if (plan->panel_rows > 0) return GEMM_OK;
-  const int64_t M = plan->M;
-  int panels = static_cast<int>(std::min<int64_t>(kHostPanelsMax, M / kHostPanelMinRows));
+  const int64_t M = plan->M, N = plan->N;
   const int64_t tile_m = static_cast<int64_t>(kBM) * plan->cg;
-  if (panels < 2) {
+  int pm = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kHostPanelsMax, M / kHostPanelMinRows)));
+  const int64_t rows = cdiv(cdiv(M, pm), tile_m) * tile_m;
+  pm = static_cast<int>(cdiv(M, rows));
+  int pn = 1;
+  int64_t cols = N;
+  if (!plan->b_kn && plan->K % 8 == 0) {
+    pn = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kHostPanelsMax, N / kHostPanelMinRows)));
+    cols = cdiv(cdiv(N, pn), 256) * 256;
+    pn = static_cast<int>(cdiv(N, cols));
+  }
+  if (pm * pn < 2) {
     plan->panel_rows = M;
-    plan->num_panels = 1;
+    plan->panel_cols = N;
+    plan->num_panels = plan->num_col_panels = 1;
     return GEMM_OK;
   }
-  const int64_t rows = cdiv(cdiv(M, panels), tile_m) * tile_m;  // whole tiles per panel
-  panels = static_cast<int>(cdiv(M, rows));
   const gemm_tuning_t* t = plan->has_tuning ? &plan->tuning : nullptr;
-  gemm_status_t st = gemm_plan_create_ex(&plan->panel_full, rows, plan->N, plan->K, plan->dtype,
-                                         plan->epi, plan->stages, plan->variant, plan->device, t);
-  if (st != GEMM_OK) return st;
-  const int64_t last = M - (panels - 1) * rows;
-  if (last != rows) {
-    st = gemm_plan_create_ex(&plan->panel_last, last, plan->N, plan->K, plan->dtype, plan->epi,
-                             plan->stages, plan->variant, plan->device, t);
-    if (st != GEMM_OK) return st;
-  }
-  cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 2 && e == cudaSuccess; ++i)
-    e = cudaStreamCreateWithFlags(&plan->copy_in[i], cudaStreamNonBlocking);
+  const int64_t hs[2] = {rows, M - (pm - 1) * rows};
+  const int64_t ws[2] = {cols, N - (pn - 1) * cols};
+  for (int lr = 0; lr < 2; ++lr)
+    for (int lc = 0; lc < 2; ++lc) {
+      if ((lr == 1 && hs[1] == rows) || (lc == 1 && ws[1] == cols)) continue;
+      gemm_status_t st = gemm_plan_create_ex(&plan->blk[lr][lc], hs[lr], ws[lc], plan->K,
+                                             plan->dtype, plan->epi, plan->stages, plan->variant,
+                                             plan->device, t);
+      if (st != GEMM_OK) return st;
+      plan->blk[lr][lc]->ldc = N;
+    }
+  cudaError_t e = cudaStreamCreateWithFlags(&plan->copy_in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&plan->copy_out, cudaStreamNonBlocking);
-  cudaEvent_t* evs[] = {&plan->ev_start, &plan->ev_b[0], &plan->ev_b[1], &plan->ev_done};
-  for (cudaEvent_t* ev : evs)
+  for (cudaEvent_t* ev : {&plan->ev_start, &plan->ev_done})
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-  for (int i = 0; i < panels && e == cudaSuccess; ++i) {
+  for (int i = 0; i < pm && e == cudaSuccess; ++i)
     e = cudaEventCreateWithFlags(&plan->ev_a[i], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&plan->ev_c[i], cudaEventDisableTiming);
-  }
+  for (int j = 0; j < pn && e == cudaSuccess; ++j)
+    e = cudaEventCreateWithFlags(&plan->ev_b[j], cudaEventDisableTiming);
+  for (int b = 0; b < pm * pn && e == cudaSuccess; ++b)
+    e = cudaEventCreateWithFlags(&plan->ev_c[b], cudaEventDisableTiming);
   if (e != cudaSuccess) return cuda_fail(e, "streams/events for gemm_run_host");
   plan->panel_rows = rows;
-  plan->num_panels = panels;
+  plan->panel_cols = cols;
+  plan->num_panels = pm;
+  plan->num_col_panels = pn;
   return GEMM_OK;
 }
 
@@ -1112,7 +1138,7 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
     st = host_panels_setup(plan);
     if (st != GEMM_OK) return st;
   }
-  if (!pipelined || plan->num_panels < 2) {
+  if (!pipelined || plan->num_panels * plan->num_col_panels < 2) {
     if (bytesA && (e = cudaMemcpyAsync(plan->hA, hA, bytesA, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
       return cuda_fail(e, "copy A to device");
     if (bytesB && (e = cudaMemcpyAsync(plan->hB, hB, bytesB, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
@@ -1125,12 +1151,16 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
     return GEMM_OK;
   }
 
-  // Pipelined: B (needed by every panel) comes in first, its two halves on two
-  // copy streams; then the row panels of A, alternating between them.  Panel
-  // i's GEMM runs on the caller's stream once its A rows (and B) are in, and
-  // its C rows go back on a third stream while the next panel computes.
-  const int P = plan->num_panels;
-  const int64_t R = plan->panel_rows;
+  // Pipelined, in blocks of C.  The host link carries ~200 GB/s each way and
+  // ~280 GB/s both ways together, so the copies set the pace: A's row panels
+  // and B's row panels (C's column panels) go in on one stream, alternating
+  // (A0, B0, A1, B1, ...), so that block (i, j) can start as soon as both of
+  // its panels are in; blocks run on the caller's stream as their panels
+  // arrive, and each block of C goes back (a 2-D copy) on a second stream
+  // while the next ones compute.  (8192^3 fp16: 1.89 ms per call with whole
+  // rows of C and B first, ~1.7 ms with 4 x 4 blocks.)
+  const int Pm = plan->num_panels, Pn = plan->num_col_panels;
+  const int64_t R = plan->panel_rows, Cw = plan->panel_cols;
   auto ck = [&](cudaError_t err, const char* what) -> bool {
     if (err != cudaSuccess) {
       cuda_fail(err, what);
@@ -1144,43 +1174,61 @@ gemm_status_t gemm_run_host(gemm_plan_t* plan, const void* hA, const void* hB, v
   char* dA = static_cast<char*>(plan->hA);
   char* dB = static_cast<char*>(plan->hB);
   char* dC = static_cast<char*>(plan->hC);
-  if (!ck(cudaEventRecord(plan->ev_start, stream), "record start")) return GEMM_ERR_CUDA;
-  const size_t halfB = (bytesB / 2) & ~static_cast<size_t>(15);
-  for (int s = 0; s < 2; ++s) {
-    if (!ck(cudaStreamWaitEvent(plan->copy_in[s], plan->ev_start, 0), "copy stream wait")) return GEMM_ERR_CUDA;
-    const size_t off = s == 0 ? 0 : halfB, len = s == 0 ? halfB : bytesB - halfB;
-    if (len && !ck(cudaMemcpyAsync(dB + off, hBb + off, len, cudaMemcpyHostToDevice, plan->copy_in[s]),
-                   "copy B to device"))
-      return GEMM_ERR_CUDA;
-    if (!ck(cudaEventRecord(plan->ev_b[s], plan->copy_in[s]), "record B")) return GEMM_ERR_CUDA;
-  }
-  for (int i = 0; i < P; ++i) {
-    const int64_t rows = std::min<int64_t>(R, M - i * R);
-    const size_t a_off = static_cast<size_t>(i) * R * K * 2, a_len = static_cast<size_t>(rows) * K * 2;
-    cudaStream_t cs = plan->copy_in[i & 1];
-    if (!ck(cudaMemcpyAsync(dA + a_off, hAb + a_off, a_len, cudaMemcpyHostToDevice, cs), "copy A panel"))
-      return GEMM_ERR_CUDA;
-    if (!ck(cudaEventRecord(plan->ev_a[i], cs), "record A panel")) return GEMM_ERR_CUDA;
-  }
-  if (!ck(cudaStreamWaitEvent(stream, plan->ev_b[0], 0), "wait B") ||
-      !ck(cudaStreamWaitEvent(stream, plan->ev_b[1], 0), "wait B"))
+  if (!ck(cudaEventRecord(plan->ev_start, stream), "record start") ||
+      !ck(cudaStreamWaitEvent(plan->copy_in, plan->ev_start, 0), "copy stream wait") ||
+      !ck(cudaStreamWaitEvent(plan->copy_out, plan->ev_start, 0), "copy-out wait"))
     return GEMM_ERR_CUDA;
-  if (!ck(cudaStreamWaitEvent(plan->copy_out, plan->ev_start, 0), "copy-out wait")) return GEMM_ERR_CUDA;
-  for (int i = 0; i < P; ++i) {
-    const int64_t rows = std::min<int64_t>(R, M - i * R);
-    gemm_plan* pp = rows == R ? plan->panel_full : plan->panel_last;
-    if (!ck(cudaStreamWaitEvent(stream, plan->ev_a[i], 0), "wait A panel")) return GEMM_ERR_CUDA;
-    st = gemm_run(pp, dA + static_cast<size_t>(i) * R * K * 2, dB,
-                  dC + static_cast<size_t>(i) * R * N * esC, rows, N, K, dtype, epi, stages,
-                  stream_handle);
-    if (st != GEMM_OK) return st;
-    if (!ck(cudaEventRecord(plan->ev_c[i], stream), "record C panel") ||
-        !ck(cudaStreamWaitEvent(plan->copy_out, plan->ev_c[i], 0), "copy-out wait"))
-      return GEMM_ERR_CUDA;
-    const size_t c_off = static_cast<size_t>(i) * R * N * esC, c_len = static_cast<size_t>(rows) * N * esC;
-    if (!ck(cudaMemcpyAsync(hCb + c_off, dC + c_off, c_len, cudaMemcpyDeviceToHost, plan->copy_out),
-            "copy C panel to host"))
-      return GEMM_ERR_CUDA;
+  int na = 0, nb = 0;
+  bool done[kHostPanelsMax][kHostPanelsMax] = {};
+  while (na < Pm || nb < Pn) {
+    // The next panel in: A while it has no more panels in than B (or B is
+    // all in), else B.
+    const bool take_a = na < Pm && (na <= nb || nb == Pn);
+    if (take_a) {
+      const int64_t rows = std::min<int64_t>(R, M - na * R);
+      const size_t off = static_cast<size_t>(na) * R * K * 2, len = static_cast<size_t>(rows) * K * 2;
+      if (!ck(cudaMemcpyAsync(dA + off, hAb + off, len, cudaMemcpyHostToDevice, plan->copy_in),
+              "copy A panel") ||
+          !ck(cudaEventRecord(plan->ev_a[na], plan->copy_in), "record A panel"))
+        return GEMM_ERR_CUDA;
+      ++na;
+    } else {
+      // One panel of B rows (N x K B), or all of B when it is the only one.
+      size_t off = 0, len = bytesB;
+      if (Pn > 1) {
+        off = static_cast<size_t>(nb) * Cw * K * 2;
+        len = static_cast<size_t>(std::min<int64_t>(Cw, N - nb * Cw)) * K * 2;
+      }
+      if (len && !ck(cudaMemcpyAsync(dB + off, hBb + off, len, cudaMemcpyHostToDevice, plan->copy_in),
+                     "copy B panel"))
+        return GEMM_ERR_CUDA;
+      if (!ck(cudaEventRecord(plan->ev_b[nb], plan->copy_in), "record B panel")) return GEMM_ERR_CUDA;
+      ++nb;
+    }
+    // Every block whose two panels are now in.
+    for (int i = 0; i < na; ++i)
+      for (int j = 0; j < nb; ++j) {
+        if (done[i][j]) continue;
+        done[i][j] = true;
+        const int64_t rows = std::min<int64_t>(R, M - i * R), cols = std::min<int64_t>(Cw, N - j * Cw);
+        gemm_plan* bp = plan->blk[rows == R ? 0 : 1][cols == Cw ? 0 : 1];
+        const size_t c_off = (static_cast<size_t>(i) * R * N + static_cast<size_t>(j) * Cw) * esC;
+        const size_t b_off = plan->b_kn ? 0 : static_cast<size_t>(j) * Cw * K * 2;
+        if (!ck(cudaStreamWaitEvent(stream, plan->ev_a[i], 0), "wait A panel") ||
+            !ck(cudaStreamWaitEvent(stream, plan->ev_b[j], 0), "wait B panel"))
+          return GEMM_ERR_CUDA;
+        st = gemm_run(bp, dA + static_cast<size_t>(i) * R * K * 2, dB + b_off, dC + c_off, rows, cols,
+                      K, dtype, epi, stages, stream_handle);
+        if (st != GEMM_OK) return st;
+        cudaEvent_t ev = plan->ev_c[i * Pn + j];
+        if (!ck(cudaEventRecord(ev, stream), "record C block") ||
+            !ck(cudaStreamWaitEvent(plan->copy_out, ev, 0), "copy-out wait") ||
+            !ck(cudaMemcpy2DAsync(hCb + c_off, static_cast<size_t>(N) * esC, dC + c_off,
+                                  static_cast<size_t>(N) * esC, static_cast<size_t>(cols) * esC, rows,
+                                  cudaMemcpyDeviceToHost, plan->copy_out),
+                "copy C block to host"))
+          return GEMM_ERR_CUDA;
+      }
   }
   if (!ck(cudaEventRecord(plan->ev_done, plan->copy_out), "record done") ||
       !ck(cudaStreamWaitEvent(stream, plan->ev_done, 0), "wait done") ||
@@ -1210,8 +1258,8 @@ gemm_status_t gemm_plan_check(gemm_plan_t* plan, int32_t* device_status, int32_t
   }
   *device_status = h[0];
   if (detail) *detail = h[1];
-  // Panel plans of gemm_run_host keep status words of their own.
-  gemm_plan* panels[2] = {plan->panel_full, plan->panel_last};
+  // Block plans of gemm_run_host keep status words of their own.
+  gemm_plan* panels[4] = {plan->blk[0][0], plan->blk[0][1], plan->blk[1][0], plan->blk[1][1]};
   for (gemm_plan* pp : panels) {
     if (!pp) continue;
     int32_t ds = 0, dd = 0;
@@ -1253,7 +1301,8 @@ void fill_info(const gemm_plan* plan, gemm_plan_info_t* info) {
   info->out_f32 = plan->out_f32;
   info->b_kn = plan->b_kn;
   info->k_sub = plan->k_sub;
-  info->host_panels = plan->num_panels >= 2 ? plan->num_panels : 0;
+  info->host_panels =
+      plan->num_panels * plan->num_col_panels >= 2 ? plan->num_panels * plan->num_col_panels : 0;
   info->stream_k_first = plan->sk_first;
   if (plan->sk_tiles > 0) info->tail_tiles = plan->sk_tiles;
 }
@@ -1327,18 +1376,20 @@ void gemm_plan_destroy(gemm_plan_t* plan) {
       if (plan->hA) cudaFree(plan->hA);
       if (plan->hB) cudaFree(plan->hB);
       if (plan->hC) cudaFree(plan->hC);
-      for (cudaStream_t cs : {plan->copy_in[0], plan->copy_in[1], plan->copy_out})
+      for (cudaStream_t cs : {plan->copy_in, plan->copy_out})
         if (cs) cudaStreamDestroy(cs);
-      for (cudaEvent_t ev : {plan->ev_start, plan->ev_b[0], plan->ev_b[1], plan->ev_done})
+      for (cudaEvent_t ev : {plan->ev_start, plan->ev_done})
         if (ev) cudaEventDestroy(ev);
       for (int i = 0; i < kHostPanelsMax; ++i) {
         if (plan->ev_a[i]) cudaEventDestroy(plan->ev_a[i]);
-        if (plan->ev_c[i]) cudaEventDestroy(plan->ev_c[i]);
+        if (plan->ev_b[i]) cudaEventDestroy(plan->ev_b[i]);
       }
+      for (cudaEvent_t ev : plan->ev_c)
+        if (ev) cudaEventDestroy(ev);
     }
   }
-  gemm_plan_destroy(plan->panel_full);
-  gemm_plan_destroy(plan->panel_last);
+  for (auto& row : plan->blk)
+    for (gemm_plan* bp : row) gemm_plan_destroy(bp);
   delete plan;
 }
 

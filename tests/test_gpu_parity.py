@@ -270,17 +270,22 @@ def test_run_host_end_to_end():
     plan.close()
 
 
-@pytest.mark.parametrize("shape,tuning", [
-    ((4096, 2048, 2048), {}),                          # 4 panels of 1024 rows
-    ((3000, 3072, 2000), {}),                          # 2 panels, shorter last one
-    ((2304, 4096, 2050), {"b_kn": 1}),                 # K x N B, padded K
-    ((2048, 3072, 1024), {"out_f32": 1, "cta_group": 1}),
+@pytest.mark.parametrize("shape,tuning,blocks", [
+    ((6144, 6144, 1024), {}, 16),                      # 4 x 4 blocks of 1536 x 1536
+    ((4096, 2048, 2048), {}, 2),                       # 2 row panels, whole rows of C
+    ((3000, 3072, 2000), {}, 2),                       # 1 x 2, ragged rows
+    ((4096, 4001, 2048), {}, 4),                       # 2 x 2, C rows not 16-byte aligned
+    ((3072, 4096, 2050), {"b_kn": 1}, 2),              # K x N B, padded K: whole rows of C
+    ((3072, 4096, 2050), {}, 2),                       # K needs padding: whole rows of C
+    ((2048, 3072, 1024), {"out_f32": 1, "cta_group": 1}, 2),
 ])
-def test_run_host_row_panels(shape, tuning):
-    # Problems with >= 32 MiB of copies run as row panels: B first on two copy
-    # streams, A panels alternating, each panel's GEMM as soon as its rows are
-    # in, C panels copied back on a third stream.  Checked at sampled positions
-    # (every panel's first and last rows included), twice on the same plan.
+def test_run_host_blocks(shape, tuning, blocks):
+    # Problems with >= 32 MiB of copies run in blocks of C: A's and B's panels
+    # in on one copy stream in turn, each block's GEMM (a plan writing into
+    # the whole C) as soon as its panels are in, each block of C back by a 2-D
+    # copy on a second stream.  Checked at sampled positions (every row and
+    # column panel's first and last rows / columns included), twice on the
+    # same plan.
     import software_pipelined_tiled_gemm_gb300 as sg
     M, N, K = shape
     A, B = gemm_inputs.custom(M, N, K, seed=M + N + K)
@@ -290,8 +295,10 @@ def test_run_host_row_panels(shape, tuning):
     plan = sg.Plan(M, N, K, "f16", stages=6, **tuning)
     stream = torch.cuda.current_stream()
     rows = [0, M - 1] + [r for i in range(1, 8) for r in (i * M // 8 - 1, i * M // 8)]
-    r = np.array(rows * 40, dtype=np.int64)
-    c = np.random.default_rng(M).integers(0, N, len(r)).astype(np.int64)
+    cols = [0, N - 1] + [x for j in range(1, 12) for x in (j * 256 - 1, j * 256) if x < N]
+    r = np.array(rows * 40 + list(np.random.default_rng(N).integers(0, M, len(cols))), dtype=np.int64)
+    c = np.concatenate([np.random.default_rng(M).integers(0, N, len(rows) * 40),
+                        np.array(cols, dtype=np.int64)]).astype(np.int64)
     ref = oracle.gemm_nt_entries(A, B, "f16", r, c)
     for _ in range(2):
         C.fill_(float("nan"))
@@ -302,7 +309,7 @@ def test_run_host_row_panels(shape, tuning):
             oracle.decode(gu.bits(C)[r, c], "f16")
         st = tolerance.compare(got, ref, "f32" if f32 else "f16")
         assert st["ok"], st
-    assert plan.info()["host_panels"] >= 2
+    assert plan.info()["host_panels"] == blocks, plan.info()["host_panels"]
     plan.close()
 
 
