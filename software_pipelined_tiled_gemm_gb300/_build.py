@@ -60,7 +60,7 @@ def _digest(checked: bool = False) -> str:
 
 
 KERNEL_FILES = ["gemm_kernel.cuh", "epilogue_math.cuh", "ptx.cuh", "kernel_params.h",
-                "gemm_instance.cuh",
+                "byte_shift.cuh", "gemm_instance.cuh",
                 "gemm_bn64.cu", "gemm_bn128.cu", "gemm_bn256.cu", "gemm_pair128.cu",
                 "gemm_pair256.cu"]
 
