@@ -480,37 +480,43 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
     ptx::tma_prefetch_desc(&tmB);
     if (kSplit) ptx::tma_prefetch_desc(&tmBt);
     if (p.tma_store) ptx::tma_prefetch_desc(&tmC);
-    // Warm L2 with the slices the ring will hold first (operands that do not
-    // stay in L2, see Params::l2_prefetch_first).  This runs before
-    // the wait on the previous kernel and only moves lines into L2, the
-    // device's point of coherence: a line the previous kernel still writes
-    // is updated there, and the ring's own copies are issued after the wait.
+  }
+  // Warm L2 with the slices the ring will hold first (operands that do not
+  // stay in L2, see Params::l2_prefetch_first).  The first epilogue warp,
+  // idle until the first accumulator is full, issues it before its wait on
+  // the previous kernel: it only moves lines into L2, the device's point of
+  // coherence (a line the previous kernel still writes is updated there),
+  // and the ring's own copies are issued after the producer's wait.  Issued
+  // by thread 0 before the CTA-wide set-up barrier instead, it delayed the
+  // other roles' start: skinny 64 x 8192 x 8192 back to back 26.35 -> 25.60
+  // us with it here (8192^3, the GELU layer and the ragged shape 0.2-0.4 %
+  // faster too).
+  auto prefetch_first_ring = [&]() {
     UnitIter it0(walker, walkers, p);
     Unit x0;
-    if (p.l2_prefetch_first && it0.next(p, x0)) {
-      int mb, nb;
-      tile_coords(x0.tile, p, mb, nb);
-      const bool narrow = kSplit && x0.sub >= 0;
-      const int n_width = narrow ? BN / p.tail_splits : BN;
-      const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
-      const int b_row = nb * BN + (narrow ? x0.sub * n_width : 0) + static_cast<int>(rank) * (n_width / CG);
-      const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
-      const int nk = x0.k1 - x0.k0;
-      const int kr = k_start(x0, walker, walkers, p);
-      for (int i = 0; i < S && i < nk; ++i) {
-        const int kb = x0.k0 + (kr + i) % nk;
+    if (!it0.next(p, x0)) return;
+    int mb, nb;
+    tile_coords(x0.tile, p, mb, nb);
+    const bool narrow = kSplit && x0.sub >= 0;
+    const int n_width = narrow ? BN / p.tail_splits : BN;
+    const int a_row = mb * kTileM + static_cast<int>(rank) * kBM;
+    const int b_row = nb * BN + (narrow ? x0.sub * n_width : 0) + static_cast<int>(rank) * (n_width / CG);
+    const void* tmb = narrow ? static_cast<const void*>(&tmBt) : static_cast<const void*>(&tmB);
+    const int nk = x0.k1 - x0.k0;
+    const int kr = k_start(x0, walker, walkers, p);
+    for (int i = 0; i < S && i < nk; ++i) {
+      const int kb = x0.k0 + (kr + i) % nk;
 #pragma unroll
-        for (int sub = 0; sub < kSub; ++sub) {
-          const int kx = (kb * kSub + sub) * kBK;
-          ptx::tma_prefetch_l2_2d(&tmA, kx, a_row);
-          if constexpr (!kKN)
-            ptx::tma_prefetch_l2_2d(tmb, kx, b_row);
-          else
-            ptx::tma_prefetch_l2_4d(tmb, 0, 0, b_row / 64, kx / 8);
-        }
+      for (int sub = 0; sub < kSub; ++sub) {
+        const int kx = (kb * kSub + sub) * kBK;
+        ptx::tma_prefetch_l2_2d(&tmA, kx, a_row);
+        if constexpr (!kKN)
+          ptx::tma_prefetch_l2_2d(tmb, kx, b_row);
+        else
+          ptx::tma_prefetch_l2_4d(tmb, 0, 0, b_row / 64, kx / 8);
       }
     }
-  }
+  };
   if (warp == 1) {
     ptx::tmem_alloc<CG>(ptx::smem_addr(tmem_slot), tmem_cols);
     ptx::tmem_relinquish<CG>();
@@ -735,6 +741,7 @@ __global__ void __launch_bounds__(kernel_threads(kEpiG), 1)
     // Warp 2 + e: TMEM lane quarter q (rows q*32 .. q*32+31 of the CTA's
     // accumulator) and column group g = e / 4 of every unit.  Stream-K
     // partials, flags and fix-up barriers are per warp e.
+    if (warp == 2 && lane == 0 && p.l2_prefetch_first) prefetch_first_ring();
     ptx::pdl_wait_prior_grid();  // bias, workspace, flags and C are global
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     const int ew = warp - 2;      // epilogue warp index: staging, partials, flags
